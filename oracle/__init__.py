@@ -1,0 +1,120 @@
+"""fp64 CPU oracle for the fused attention forward pass -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path never does.
+
+The arithmetic lives in ``attn_ref.cpp`` (plain float64 C++, one materialised
+score row per query, two-pass softmax).  This module compiles it with the host
+C++ compiler on first use (or from ``build()``) and calls it through ctypes.
+The functions here only marshal arguments.
+
+Parity pins: ``tests/test_oracle_pins.py`` and ``tests/test_oracle_mutants.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+SOURCE = _HERE / "attn_ref.cpp"
+BUILD_DIR = _HERE / "_build"
+LIB_PATH = BUILD_DIR / "libattn_ref.so"
+
+_lib = None
+
+
+def compile_library(source: Path = SOURCE, out: Path = LIB_PATH, extra_flags=()) -> Path:
+    """Compile ``source`` into the shared library ``out`` (atomic rename)."""
+    out.parent.mkdir(parents=True, exist_ok=True)
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=str(out.parent))
+    os.close(fd)
+    cmd = ["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-pthread",
+           *extra_flags, str(source), "-o", tmp]
+    try:
+        subprocess.run(cmd, check=True, capture_output=True, text=True)
+    except subprocess.CalledProcessError as e:
+        os.unlink(tmp)
+        raise RuntimeError(f"oracle build failed:\n{e.stderr}") from e
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> Path:
+    """Build the oracle library if it is missing or older than its source."""
+    if force or not LIB_PATH.exists() or LIB_PATH.stat().st_mtime < SOURCE.stat().st_mtime:
+        compile_library()
+    return LIB_PATH
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    i64, p = ctypes.c_int64, ctypes.c_void_p
+    lib.attn_ref_f64.restype = ctypes.c_int
+    lib.attn_ref_f64.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_double,
+                                 ctypes.c_int, p, p, i64, p, p, ctypes.c_int]
+    lib.attn_ref_score_buffer_bytes.restype = ctypes.c_uint64
+    lib.attn_ref_score_buffer_bytes.argtypes = [i64, i64, i64, i64]
+    lib.attn_ref_hardware_threads.restype = ctypes.c_int
+    lib.attn_ref_hardware_threads.argtypes = []
+    return lib
+
+
+def load_library(path: Path | None = None) -> ctypes.CDLL:
+    """Load the default oracle library (building it if needed), or ``path``."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(str(path)))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(str(build())))
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def attention_f64(q_bits, k_bits, v_bits, scale: float, causal: bool,
+                  kv_valid_len=None, rows=None, threads: int = 0, lib=None):
+    """Reference O and LSE in float64.
+
+    q_bits: uint16 bf16 bits [B,H,S_q,D]; k_bits, v_bits: [B,H,S_kv,D].
+    kv_valid_len: ints of length B or None.  rows: flat row ids
+    ``(b*H + h)*S_q + i`` or None for all rows.
+    Returns (o [n_rows, D] float64, lse [n_rows] float64).
+    """
+    lib = lib or load_library()
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    B, H, S_q, D = q.shape
+    S_kv = k.shape[2]
+    if k.shape != (B, H, S_kv, D) or v.shape != k.shape:
+        raise ValueError("shape mismatch")
+    kvl = None if kv_valid_len is None else np.ascontiguousarray(kv_valid_len, dtype=np.int32)
+    if kvl is not None and kvl.shape != (B,):
+        raise ValueError("kv_valid_len must have one entry per batch")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n_rows = B * H * S_q if r is None else int(r.shape[0])
+    o = np.empty((n_rows, D), dtype=np.float64)
+    lse = np.empty((n_rows,), dtype=np.float64)
+    rc = lib.attn_ref_f64(_ptr(q), _ptr(k), _ptr(v), B, H, S_q, S_kv, D, float(scale),
+                          int(bool(causal)), _ptr(kvl), _ptr(r), n_rows, _ptr(o), _ptr(lse),
+                          int(threads))
+    if rc != 0:
+        raise ValueError(f"attn_ref_f64 rejected its arguments (rc={rc})")
+    return o, lse
+
+
+def score_buffer_bytes(B: int, H: int, s: int, e: int, lib=None) -> int:
+    """Bytes of a materialised B x H x s x s score matrix, e bytes per score."""
+    lib = lib or load_library()
+    return int(lib.attn_ref_score_buffer_bytes(B, H, s, e))
+
+
+def hardware_threads(lib=None) -> int:
+    lib = lib or load_library()
+    return int(lib.attn_ref_hardware_threads())

@@ -1,0 +1,153 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the smoke check.
+
+This module only draws numbers. It holds none of the attention arithmetic, so
+both the CPU oracle and the CUDA path can take their inputs from here without
+sharing any of the computation under test.
+
+Generator (counter-based, so any element can be drawn independently):
+
+* SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+  generators", OOPSLA 2014) in its counter form: word ``n`` of a stream with
+  state ``s0`` is ``mix64(s0 + (n + 1) * GAMMA)`` with
+  ``GAMMA = 0x9E3779B97F4A7C15`` and ``mix64`` the SplitMix64 finaliser.
+* A stream is keyed by ``(seed, tensor_id)``:
+  ``s0 = mix64(seed * GAMMA + tensor_id)``.
+* Uniforms on the open interval (0, 1): ``((w >> 11) + 0.5) * 2**-53``.
+* Standard normals by Box-Muller (1958) in float64: element pair ``m`` uses
+  words ``2m`` and ``2m + 1``; ``r = sqrt(-2 ln u1)``, ``theta = 2 pi u2``;
+  element ``2m`` is ``r cos theta`` and element ``2m + 1`` is ``r sin theta``.
+* bf16 values: the float64 normal is rounded to float32 (round to nearest
+  even), then to bf16 (round to nearest even).  A multiplier that is a power
+  of two (the peaked and long-context workloads) is applied to the bf16 value
+  exactly, so every consumer sees the same bits.
+
+Tensors are returned as ``numpy.uint16`` arrays of bf16 bit patterns, laid out
+``[B][H][S][D]`` row-major.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+# Tensor ids of the streams drawn for one workload.
+TID_Q, TID_K, TID_V, TID_ROWS = 1, 2, 3, 4
+
+_CHUNK = 1 << 22  # elements drawn per vectorised chunk (bounds temporaries)
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    """SplitMix64 finaliser on a uint64 array (wrapping arithmetic)."""
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def _stream_state(seed: int, tensor_id: int) -> np.uint64:
+    with np.errstate(over="ignore"):
+        s = np.array([seed], dtype=np.uint64) * GAMMA + np.uint64(tensor_id)
+        return _mix64(s)[0]
+
+
+def uniform_words(seed: int, tensor_id: int, start: int, count: int) -> np.ndarray:
+    """Words ``start .. start+count-1`` of stream (seed, tensor_id) as uint64."""
+    s0 = _stream_state(seed, tensor_id)
+    n = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix64(s0 + n * GAMMA)
+
+
+def _words_to_unit(w: np.ndarray) -> np.ndarray:
+    return ((w >> np.uint64(11)).astype(np.float64) + 0.5) * (2.0 ** -53)
+
+
+def normal_f64(seed: int, tensor_id: int, count: int, start: int = 0) -> np.ndarray:
+    """``count`` standard normals (float64) from element ``start`` of the stream.
+
+    ``start`` must be even so that Box-Muller pairs line up.
+    """
+    if start % 2:
+        raise ValueError("start must be even")
+    npairs = (count + 1) // 2
+    w = uniform_words(seed, tensor_id, start, 2 * npairs)
+    u1 = _words_to_unit(w[0::2])
+    u2 = _words_to_unit(w[1::2])
+    r = np.sqrt(-2.0 * np.log(u1))
+    th = (2.0 * math.pi) * u2
+    out = np.empty(2 * npairs, dtype=np.float64)
+    out[0::2] = r * np.cos(th)
+    out[1::2] = r * np.sin(th)
+    return out[:count]
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest even); returns uint16 bit patterns.
+
+    Inputs here are finite; NaN handling is not needed.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounding = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + rounding) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float32 exactly."""
+    return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal_bf16(seed: int, tensor_id: int, count: int, multiplier: float = 1.0) -> np.ndarray:
+    """``count`` N(0,1) draws rounded to bf16, times an exact power of two."""
+    if multiplier != 1.0:
+        m, e = math.frexp(multiplier)
+        if m != 0.5:
+            raise ValueError("multiplier must be a power of two")
+    out = np.empty(count, dtype=np.uint16)
+    for lo in range(0, count, _CHUNK):
+        n = min(_CHUNK, count - lo)
+        x = normal_f64(seed, tensor_id, n, start=lo).astype(np.float32)
+        bits = f32_to_bf16_bits(x)
+        if multiplier != 1.0:
+            bits = f32_to_bf16_bits(bf16_bits_to_f32(bits) * np.float32(multiplier))
+        out[lo:lo + n] = bits
+    return out
+
+
+def qkv_bf16(seed: int, B: int, H: int, S_q: int, S_kv: int, D: int,
+             q_mult: float = 1.0, k_mult: float = 1.0):
+    """Q, K, V of one workload as uint16 bf16 bits, shapes [B,H,S,D]."""
+    q = normal_bf16(seed, TID_Q, B * H * S_q * D, q_mult).reshape(B, H, S_q, D)
+    k = normal_bf16(seed, TID_K, B * H * S_kv * D, k_mult).reshape(B, H, S_kv, D)
+    v = normal_bf16(seed, TID_V, B * H * S_kv * D).reshape(B, H, S_kv, D)
+    return q, k, v
+
+
+def sample_rows(seed: int, S: int, n: int, must_include=()) -> np.ndarray:
+    """``n`` distinct row indices in [0, S) (sorted), always holding ``must_include``.
+
+    Rows come from stream (seed, TID_ROWS): a partial Fisher-Yates shuffle of
+    0..S-1 driven by its words.
+    """
+    n = min(n, S)
+    chosen = [r for r in dict.fromkeys(int(r) for r in must_include) if 0 <= r < S]
+    pool = {}
+    words = uniform_words(seed, TID_ROWS, 0, S if S < 4 * n else 4 * n)
+    picked = set(chosen)
+    wi = 0
+    i = 0
+    while len(chosen) < n:
+        # swap position i with a uniform j in [i, S)
+        j = i + int(words[wi % len(words)] % np.uint64(S - i))
+        wi += 1
+        vi, vj = pool.get(i, i), pool.get(j, j)
+        pool[i], pool[j] = vj, vi
+        i += 1
+        if vj not in picked:
+            picked.add(vj)
+            chosen.append(vj)
+        if i >= S:
+            break
+    return np.array(sorted(chosen[:n]), dtype=np.int64)
