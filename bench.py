@@ -1,0 +1,440 @@
+"""Benchmark of the fused attention forward pass on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                [--workload NAME]
+
+Prints ONE JSON line (rank 0).  A step is one forward pass of the workload in
+every mode it lists (e.g. non-causal and causal), i.e. the whole kernel path:
+tile schedule, TMA loads, QK^T and PV on the tensor cores, masking, online
+softmax, lazy correction and the epilogue.
+
+  value            algorithmic TFLOP/s (4 * D * allowed query-key pairs per
+                   mode) with inputs resident in HBM, CUDA-event timed on the
+                   launching stream, L2 flushed (256 MiB write) before every
+                   step, summed over ranks / max time over ranks.
+  e2e              the same metric through the C ABI with host buffers:
+                   pinned host -> device copies of Q, K, V and device -> host
+                   copies of O and LSE inside the timed region.
+  roofline         for the attention kernel (the only kernel in a step):
+                   achieved = algorithmic FLOPs per launch / mean launch time,
+                   against the measured dense bf16 peak.
+  cpu_baseline     the fp64 CPU oracle on a bounded sample of the same
+                   workload, timed on the host cores (rank 0, N = 1 only).
+
+With N > 1 (torchrun) every rank runs its own replica (the path has no
+exchange step): scaling is weak.  --impl reference times the oracle instead
+(rank 0 only; other ranks exit at once).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+METRIC = "attention fwd TFLOP/s (bf16) and % of GB300 tensor-core peak, s=1k–32k"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAK_TFLOPS = 1900.0
+
+# name -> B, H, S (S_q = S_kv), D, modes (causal flags), seed, q/k multipliers, kv_valid_len
+WORKLOADS = {
+    "b4_h16_s1024_d64": dict(B=4, H=16, S=1024, D=64, modes=(False, True), seed=2),
+    "b4_h16_s1024_d64_qx8": dict(B=4, H=16, S=1024, D=64, modes=(False, True), seed=3, q_mult=8.0),
+    "b1_h32_s4096_d128": dict(B=1, H=32, S=4096, D=128, modes=(True, False), seed=4),
+    "b2_h32_s8192_d128_padded": dict(B=2, H=32, S=8192, D=128, modes=(False,), seed=5,
+                                     valid=(8192, 5000)),
+    "b1_h32_s32768_d128_qkx2": dict(B=1, H=32, S=32768, D=128, modes=(True, False), seed=6,
+                                    q_mult=2.0, k_mult=2.0),
+}
+DEFAULT_WORKLOAD = "b4_h16_s1024_d64"
+
+
+def allowed_pairs(B, H, S_q, S_kv, causal, valid=None):
+    """Number of allowed (query, key) pairs of one forward pass."""
+    total = 0
+    for b in range(B):
+        n = S_kv if valid is None else max(0, min(valid[b], S_kv))
+        if causal:
+            # row i sees min(n, i + 1) keys
+            m = min(S_q, n)
+            per_head = m * (m + 1) // 2 + (S_q - m) * n
+        else:
+            per_head = S_q * n
+        total += H * per_head
+    return total
+
+
+def alg_flops(w, causal):
+    return 4 * w["D"] * allowed_pairs(w["B"], w["H"], w["S"], w["S"], causal, w.get("valid"))
+
+
+def alg_bytes(w, causal):
+    """Q + valid K/V + O (bf16) + LSE (fp32) of one forward pass."""
+    B, H, S, D = w["B"], w["H"], w["S"], w["D"]
+    kv = sum(min(w["valid"][b], S) if w.get("valid") else S for b in range(B))
+    return H * (2 * S * D * 2 * B + 2 * kv * D * 2 + S * 4 * B)
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+        except (ValueError, KeyError):
+            pass
+    return FALLBACK_PEAK_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst)"
+
+
+def kernel_source_hash():
+    src = ROOT / "io_aware_attention_fwd_gb300" / "csrc" / "attn_fwd.cu"
+    return hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    prof = ROOT / "profiles"
+    if not prof.is_dir():
+        return None
+    for f in sorted(prof.glob("*.md")):
+        text = f.read_text()
+        m_w = re.search(r"^bench_workload:\s*(\S+)", text, re.M)
+        m_h = re.search(r"^kernel_source_sha256_16:\s*(\S+)", text, re.M)
+        m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        if m_w and m_h and m_t and m_w.group(1) == workload and m_h.group(1) == kernel_source_hash():
+            return float(m_t.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in Path(self.path).read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        busy = [r for r in rows if r[2] > 0.35 * max(x[2] for x in rows)] or rows
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in busy:
+            for name, flag in zip(names, r[3]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy)}
+
+
+def oracle_sample(w, q_bits, k_bits, v_bits, target_s, modes):
+    """Time the fp64 oracle on a bounded row sample of the workload.
+
+    Rows are spread evenly over all heads and positions; the per-mode FLOPs of
+    exactly those rows are credited.  Returns (TFLOP/s, seconds, rows, threads).
+    """
+    import numpy as np
+    import oracle
+
+    B, H, S, D = w["B"], w["H"], w["S"], w["D"]
+    valid = w.get("valid")
+    scale = 1.0 / math.sqrt(D)
+    total_rows = B * H * S
+    threads = oracle.hardware_threads()
+
+    def row_flops(rows, causal):
+        b = rows // (H * S)
+        i = rows % S
+        n = np.full(rows.shape, S) if valid is None else np.asarray(valid)[b]
+        keys = np.minimum(n, i + 1) if causal else n
+        return 4.0 * D * float(keys.sum())
+
+    def run(nrows):
+        rows = np.unique(np.linspace(0, total_rows - 1, nrows).astype(np.int64))
+        t0 = time.perf_counter()
+        fl = 0.0
+        for causal in modes:
+            oracle.attention_f64(q_bits, k_bits, v_bits, scale, causal, kv_valid_len=valid, rows=rows,
+                                 threads=threads)
+            fl += row_flops(rows, causal)
+        return fl, time.perf_counter() - t0, len(rows)
+
+    nrows = min(total_rows, 64)
+    fl, dt, n = run(nrows)
+    if n < total_rows and dt < target_s:
+        nrows = int(min(total_rows, max(nrows, nrows * target_s / max(dt, 1e-3))))
+        fl, dt, n = run(nrows)
+    return fl / dt / 1e12, dt, n, threads
+
+
+def cpu_model():
+    try:
+        for line in Path("/proc/cpuinfo").read_text().splitlines():
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def run_reference(args, w, rank):
+    """--impl reference: the oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return 0
+    import numpy as np
+    import seeded_inputs as si
+
+    q, k, v = si.qkv_bf16(w["seed"], w["B"], w["H"], w["S"], w["S"], w["D"],
+                          w.get("q_mult", 1.0), w.get("k_mult", 1.0))
+    per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, per_step, w["modes"])
+    vals, secs, rows, threads = [], 0.0, 0, 1
+    for _ in range(args.steps):
+        tf, dt, rows, threads = oracle_sample(w, q, k, v, per_step, w["modes"])
+        vals.append(tf)
+        secs += dt
+    value = statistics.median(vals)
+    sample = (f"{rows} of {w['B'] * w['H'] * w['S']} query rows per step (evenly spaced over heads and "
+              f"positions), modes {['causal' if c else 'non-causal' for c in w['modes']]}; "
+              f"TFLOP/s credited for exactly those rows")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 inputs)",
+        "config": {"workload": args.workload, **{k_: w[k_] for k_ in ("B", "H", "S", "D")},
+                   "modes": ["causal" if c else "non-causal" for c in w["modes"]]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample, "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target oracle time for the cpu_baseline sample (0 disables)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, w, rank)
+
+    import torch
+    import io_aware_attention_fwd_gb300 as attn
+    import seeded_inputs as si
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    attn.load()
+
+    B, H, S, D = w["B"], w["H"], w["S"], w["D"]
+    modes = w["modes"]
+    scale = 1.0 / math.sqrt(D)
+    q, k, v = si.qkv_bf16_torch(w["seed"], B, H, S, S, D, w.get("q_mult", 1.0), w.get("k_mult", 1.0),
+                                device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    kvl = torch.tensor(w["valid"], dtype=torch.int32, device=dev) if w.get("valid") else None
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def launch(causal):
+        attn.attn_fwd(q, k, v, o, lse, B, H, S, S, D, scale, causal, kvl, stream)
+
+    # host buffers for the end-to-end leg
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = (ho.numel() * ho.element_size() + hl.numel() * hl.element_size()) * len(modes)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        for causal in modes:
+            launch(causal)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        for causal in modes:
+            launch(causal)
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    st = attn.attn_fwd_debug_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"device status after warm-up: {attn.attn_status_str(st)}")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    # keep the GPU busy for ~1 s before timing so clock samples see load
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        for causal in modes:
+            launch(causal)
+        torch.cuda.synchronize(dev)
+
+    n_l = len(modes)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_l + 1)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, causal in enumerate(modes):
+            launch(causal)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    step_ms = [ev[i][0].elapsed_time(ev[i][n_l]) for i in range(args.steps)]
+    launch_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(n_l)]
+
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        e_ev[i][0].record(stream)
+        e2e_step()
+        e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    e2e_ms = [a.elapsed_time(b) for a, b in e_ev]
+    st = attn.attn_fwd_debug_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"device status after timing: {attn.attn_status_str(st)}")
+
+    flops_step = sum(alg_flops(w, c) for c in modes)
+    t_step = sum(step_ms) / len(step_ms)
+    t_e2e = sum(e2e_ms) / len(e2e_ms)
+    if dist is not None:
+        t = torch.tensor([t_step, t_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step, t_e2e = float(t[0]), float(t[1])
+    value = world * flops_step / (t_step * 1e-3) / 1e12
+    e2e_value = world * flops_step / (t_e2e * 1e-3) / 1e12
+
+    # roofline of the attention kernel: every launch in the step is attn_fwd_sm103a<D>
+    mean_launch_ms = sum(sum(x) for x in launch_ms) / (args.steps * n_l)
+    flops_launch = flops_step / n_l
+    peak, peak_src = load_peaks()
+    achieved = flops_launch / (mean_launch_ms * 1e-3) / 1e12
+    per_mode = {("causal" if c else "non-causal"): {
+        "ms": sum(launch_ms[j]) / args.steps,
+        "tflops": alg_flops(w, c) / (sum(launch_ms[j]) / args.steps * 1e-3) / 1e12,
+        "frac_of_peak": alg_flops(w, c) / (sum(launch_ms[j]) / args.steps * 1e-3) / 1e12 / peak,
+    } for j, c in enumerate(modes)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V drawn on the device)",
+        "config": {"workload": args.workload, "B": B, "H": H, "S_q": S, "S_kv": S, "D": D,
+                   "scale": scale, "modes": ["causal" if c else "non-causal" for c in modes],
+                   "kv_valid_len": list(w["valid"]) if w.get("valid") else None,
+                   "q_mult": w.get("q_mult", 1.0), "k_mult": w.get("k_mult", 1.0),
+                   "l2": "flushed before every timed step (256 MiB device write)",
+                   "parallelism": f"replicas x{world}"},
+        "per_mode": per_mode,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                     "alg_bytes_per_launch": sum(alg_bytes(w, c) for c in modes) / n_l,
+                     "kernel": f"attn_fwd_sm103a<{D}>", "peak_source": peak_src},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * n_l,
+        "clocks": clocks,
+    }
+
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        import numpy as np
+        hb = [x.view(torch.int16).numpy().view(np.uint16) for x in (hq, hk, hv)]
+        tf, dt, rows, threads = oracle_sample(w, *hb, args.cpu_seconds, modes)
+        line["cpu_baseline"] = {
+            "value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": (f"{rows} of {B * H * S} query rows (evenly spaced over heads and positions), "
+                       f"each in modes {line['config']['modes']}, {dt:.1f} s of fp64 CPU time; "
+                       f"TFLOP/s credited for exactly those rows"),
+            "cpu": cpu_model(),
+        }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

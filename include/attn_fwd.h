@@ -1,0 +1,105 @@
+/*
+ * attn_fwd.h -- C ABI of the fused scaled-dot-product attention forward pass
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (per batch b, head h, query row i):
+ *
+ *     s_ij   = scale * <q_i, k_j>                  for allowed keys j
+ *     O_i    = sum_j softmax_j(s_i.) * v_j
+ *     LSE_i  = ln sum_{allowed j} exp(s_ij)
+ *
+ *   - "Attention memory" page (onecalc.app), sections "The quadratic bound"
+ *     and "What this memory is": entry (i, j) of the s x s score matrix is how
+ *     much token i attends to token j; it sits between the query-key product
+ *     and the softmax-weighted sum of the values.
+ *   - Same page, section "FlashAttention", and the "Flash attention" glossary
+ *     page (news.hamidun.com), second paragraph: the output is built block by
+ *     block over the keys and values with running softmax statistics, so the
+ *     s x s matrix is never written to HBM.  This library allocates nothing;
+ *     its working set is on-chip (shared memory and tensor memory).
+ *   - "PyTorch attention backends" story (hyper.ai), masked_fill sentences:
+ *     a masked key is filled with -inf before the softmax.  Key j is allowed
+ *     for row i iff j < S_kv, j < kv_valid_len[b] (when given) and, if causal,
+ *     j <= i (top-left alignment, as torch's is_causal).  The mask is never
+ *     materialised; it is evaluated from indices inside the kernel.
+ *   - A row with no allowed key gets O_i = 0 and LSE_i = -inf.
+ *
+ * Layout: q, o are bf16 [B][H][S_q][D]; k, v are bf16 [B][H][S_kv][D]; lse is
+ * fp32 [B][H][S_q]; all contiguous, row-major.  D is 64 or 128.
+ */
+#ifndef ATTN_FWD_H_
+#define ATTN_FWD_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, scale not finite and > 0 */
+  ATTN_ERR_UNSUPPORTED = 2,  /* D not 64/128, device not sm_103, size beyond limits */
+  ATTN_ERR_ALIGNMENT = 3,    /* q/k/v/o not 16-byte aligned, lse/kv_valid_len not 4-byte */
+  ATTN_ERR_LAUNCH = 4,       /* the CUDA launch (or tensor-map encoding) failed */
+  ATTN_ERR_TIMEOUT = 5,      /* a bounded in-kernel wait gave up (see attn_fwd_debug_status) */
+  ATTN_ERR_DEVICE = 6        /* CUDA runtime / driver error outside the launch */
+} attn_status_t;
+
+/*
+ * attn_fwd -- enqueue the attention forward pass on `stream`.
+ *
+ *   q, k, v       device pointers, bf16, layouts above, 16-byte aligned.
+ *   o             device pointer, bf16 [B][H][S_q][D], written.
+ *   lse           device pointer, fp32 [B][H][S_q], written (natural log).
+ *                 q, o, lse may be NULL when S_q == 0; k, v may be NULL when
+ *                 S_kv == 0 (then every row gets O = 0, LSE = -inf).
+ *   B, H          >= 1.  S_q, S_kv >= 0 (S_q == 0 is a no-op).
+ *   D             64 or 128.
+ *   scale         finite and > 0 (usually 1/sqrt(D)).
+ *   causal        0 or 1.
+ *   kv_valid_len  device int32[B] or NULL (NULL means S_kv for every batch).
+ *                 The host never reads it; the kernel clamps each entry to
+ *                 [0, S_kv].
+ *   stream        a cudaStream_t (NULL = legacy default stream).
+ *
+ * Asynchronous: returns once the kernel is enqueued.  Every argument check
+ * happens before anything is launched; on an error nothing is enqueued and
+ * the outputs are untouched.  The caller owns every buffer; the library
+ * allocates no device memory.  Thread-safe.  Inputs and outputs must not
+ * overlap.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int S_q, int S_kv, int D, float scale, int causal,
+                       const int32_t* kv_valid_len, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* attn_status_str(attn_status_t status);
+
+/*
+ * attn_fwd_debug_status -- synchronise `stream`, then read and clear the
+ * device status word that the kernels set when a bounded wait gives up.
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_DEVICE if the
+ * synchronisation itself reported a CUDA error.
+ */
+attn_status_t attn_fwd_debug_status(void* stream);
+
+/*
+ * attn_watchdog_selftest -- launch a one-warp kernel that waits on a shared
+ * memory barrier nothing ever completes, with the same bounded wait the
+ * attention kernel uses and a limit of `timeout_ns` nanoseconds
+ * (1e3 .. 1e10).  The kernel gives up, records the timeout and returns; this
+ * call then synchronises `stream` and returns what attn_fwd_debug_status
+ * returns (ATTN_ERR_TIMEOUT when the watchdog works).  Not part of the
+ * attention computation: it exercises the failure path without a GPU fault.
+ */
+attn_status_t attn_watchdog_selftest(uint64_t timeout_ns, void* stream);
+
+/* Version of this ABI (incremented on incompatible change). */
+int attn_fwd_abi_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* ATTN_FWD_H_ */

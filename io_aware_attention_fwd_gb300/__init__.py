@@ -1,0 +1,20 @@
+"""Fused scaled-dot-product attention forward for GB300 (sm_103a).
+
+``attn_fwd`` and friends mirror the C ABI of ``include/attn_fwd.h``;
+``attention_forward`` is a tensor-level convenience wrapper.  The CUDA
+library is loaded on first use and must have been built (``build_ext``).
+"""
+from ._lib import (ATTN_ERR_ALIGNMENT, ATTN_ERR_DEVICE, ATTN_ERR_INVALID_ARG, ATTN_ERR_LAUNCH,
+                   ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED, ATTN_OK, EXPORTED, AttnError, attn_fwd,
+                   attn_fwd_abi_version, attn_fwd_debug_status, attn_fwd_status, attn_status_str,
+                   attn_watchdog_selftest, load)
+from .api import attention_forward
+from .build_ext import LIB_PATH, build
+
+__all__ = [
+    "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_ALIGNMENT",
+    "ATTN_ERR_LAUNCH", "ATTN_ERR_TIMEOUT", "ATTN_ERR_DEVICE", "EXPORTED", "AttnError",
+    "attn_fwd", "attn_fwd_status", "attn_status_str", "attn_fwd_debug_status",
+    "attn_watchdog_selftest", "attn_fwd_abi_version", "attention_forward", "load", "build",
+    "LIB_PATH",
+]

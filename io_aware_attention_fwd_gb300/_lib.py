@@ -1,0 +1,116 @@
+"""ctypes binding of the C ABI declared in ``include/attn_fwd.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  If the library has not been built, calls raise ``RuntimeError``;
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from .build_ext import LIB_PATH
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_ALIGNMENT = 3
+ATTN_ERR_LAUNCH = 4
+ATTN_ERR_TIMEOUT = 5
+ATTN_ERR_DEVICE = 6
+
+# every extern "C" function include/attn_fwd.h declares
+EXPORTED = ("attn_fwd", "attn_status_str", "attn_fwd_debug_status",
+            "attn_watchdog_selftest", "attn_fwd_abi_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero attn_status_t returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {attn_status_str(status)} (status {status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load the built library (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not LIB_PATH.exists():
+                raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                                   "(run __graft_entry__.build() or "
+                                   "python -m io_aware_attention_fwd_gb300.build_ext)")
+            lib = ctypes.CDLL(str(LIB_PATH))
+            p, i = ctypes.c_void_p, ctypes.c_int
+            lib.attn_fwd.restype = i
+            lib.attn_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p, p]
+            lib.attn_status_str.restype = ctypes.c_char_p
+            lib.attn_status_str.argtypes = [i]
+            lib.attn_fwd_debug_status.restype = i
+            lib.attn_fwd_debug_status.argtypes = [p]
+            lib.attn_watchdog_selftest.restype = i
+            lib.attn_watchdog_selftest.argtypes = [ctypes.c_uint64, p]
+            lib.attn_fwd_abi_version.restype = i
+            lib.attn_fwd_abi_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _addr(x):
+    """Device address of a tensor-like (``data_ptr()``) or a plain int/None."""
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return int(s)
+
+
+def attn_status_str(status: int) -> str:
+    return load().attn_status_str(int(status)).decode()
+
+
+def attn_fwd(q, k, v, o, lse, B: int, H: int, S_q: int, S_kv: int, D: int, scale: float,
+             causal: bool, kv_valid_len=None, stream=None) -> None:
+    """Enqueue the attention forward pass (see include/attn_fwd.h).
+
+    q, k, v, o, lse, kv_valid_len: device buffers (tensors or raw addresses).
+    Raises AttnError on a non-zero status.
+    """
+    st = load().attn_fwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
+                         int(S_q), int(S_kv), int(D), float(scale), int(bool(causal)),
+                         _addr(kv_valid_len), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+
+
+def attn_fwd_status(*args, **kwargs) -> int:
+    """Same as attn_fwd but returns the raw status instead of raising."""
+    try:
+        attn_fwd(*args, **kwargs)
+    except AttnError as e:
+        return e.status
+    return ATTN_OK
+
+
+def attn_fwd_debug_status(stream=None) -> int:
+    return int(load().attn_fwd_debug_status(_stream(stream)))
+
+
+def attn_watchdog_selftest(timeout_ns: int, stream=None) -> int:
+    return int(load().attn_watchdog_selftest(int(timeout_ns), _stream(stream)))
+
+
+def attn_fwd_abi_version() -> int:
+    return int(load().attn_fwd_abi_version())

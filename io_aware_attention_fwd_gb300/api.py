@@ -1,0 +1,44 @@
+"""Tensor-level convenience wrapper over the C ABI.
+
+PyTorch only provides the device memory and the stream here; the computation
+is the CUDA library's.
+"""
+from __future__ import annotations
+
+import math
+
+from . import _lib
+
+
+def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
+                      kv_valid_len=None, out=None, lse=None, stream=None):
+    """O and LSE for bf16 CUDA tensors q [B,H,S_q,D], k/v [B,H,S_kv,D].
+
+    kv_valid_len: int32 CUDA tensor [B] or None.  Returns (o, lse) with o bf16
+    [B,H,S_q,D] and lse fp32 [B,H,S_q].
+    """
+    import torch
+
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k, v must be bfloat16")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous [B,H,S,D]")
+    B, H, S_q, D = q.shape
+    S_kv = k.shape[2]
+    if tuple(k.shape) != (B, H, S_kv, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B,H,S_kv,D] matching q")
+    if kv_valid_len is not None:
+        if kv_valid_len.dtype != torch.int32 or not kv_valid_len.is_cuda or kv_valid_len.numel() != B:
+            raise ValueError("kv_valid_len must be an int32 CUDA tensor with B entries")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    _lib.attn_fwd(q, k, v, out, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len, stream)
+    return out, lse

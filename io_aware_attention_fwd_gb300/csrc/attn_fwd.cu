@@ -1,0 +1,845 @@
+// Fused scaled-dot-product attention forward pass for GB300 (sm_103a).
+//
+//   O = softmax(scale * Q K^T + mask) V,   LSE = ln sum exp(scale * Q K^T + mask)
+//
+// The pages behind this kernel (cited by title and section):
+//   * "Attention memory" (onecalc.app), sections "The quadratic bound" and
+//     "What this memory is": the s x s score matrix between the query-key
+//     product and the softmax-weighted sum of values is what naive attention
+//     writes to memory.  Section "FlashAttention": walk the keys and values
+//     in small blocks, keep running softmax statistics, and never write the
+//     s x s matrix.  This kernel keeps each 128 x 128 score tile in tensor
+//     memory (TMEM) and never sends it to HBM.
+//   * "Flash attention" glossary (news.hamidun.com), second paragraph: tiles
+//     that fit on-chip, an incremental numerically stable softmax,
+//     parallelism across the sequence (the grid runs over query tiles), fewer
+//     non-matmul operations (exp2 with the scale folded in, the 1/l division
+//     deferred to the epilogue, lazy rescaling of O), and warp specialisation.
+//   * "PyTorch attention backends" story (hyper.ai), masked_fill sentences:
+//     a masked key scores -inf.  Here the causal and key-padding predicates
+//     are evaluated from indices in registers; no mask tensor exists.
+//
+// One CTA computes two 128-row query tiles of one (batch, head) against all
+// of that head's allowed keys.  Warp roles (384 threads):
+//   warp 0       TMA producer: Q tiles once, then K/V tiles into a ring of
+//                shared-memory slots guarded by mbarriers.
+//   warp 1       tcgen05.mma issuer (one thread): S_t = Q_t K_j^T into TMEM,
+//                then O_t += P_t V_j with P_t read from TMEM.
+//   warps 4-7    softmax for query tile 0; warps 8-11 for query tile 1.  One
+//                thread owns one query row (one TMEM lane): it reads its S
+//                row, masks, updates the running max and sum, writes P (bf16)
+//                back over S, rescales O lazily, and runs the epilogue.
+// While one softmax warpgroup works on its tile, the tensor core runs the
+// other tile's MMAs, so exp2 work and MMAs overlap.
+//
+// Every wait on a barrier is bounded by a %globaltimer deadline.  A wait that
+// gives up sets a shared abort flag and a device status word, and every role
+// then leaves its loop, waits (bounded) for its own copies and MMAs in
+// flight, and the CTA frees its TMEM and exits.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_fwd.h"
+
+namespace {
+
+constexpr int kBM = 128;              // query rows per softmax tile (TMEM lanes)
+constexpr int kBN = 128;              // keys per kv tile
+constexpr int kQTiles = 2;            // query tiles per CTA
+constexpr int kRowsPerCta = kBM * kQTiles;
+constexpr int kThreads = 384;         // warps 0-3: roles, 4-7 / 8-11: softmax
+constexpr uint32_t kTmemCols = 512;   // S0 | S1 | O0 | O1
+constexpr int kPanelBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kPanels = D / 64;
+  static constexpr int kTileBytes = 128 * D * 2;  // one [128 x D] bf16 tile
+  static constexpr int kSlots = (D == 128) ? 4 : 8;
+  static constexpr int kQOff = 0;
+  static constexpr int kSlotOff = kQTiles * kTileBytes;
+  static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
+  // barriers: q_full | full[kSlots] | empty[kSlots] | s_full[2] | p_full[2] | o_done[2] | drain
+  static constexpr int kNumBars = 1 + 2 * kSlots + 3 * kQTiles + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] tmem base, [1] abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024 B alignment
+  static constexpr int kOCol0 = kQTiles * kBN;             // first O column in TMEM
+};
+
+struct Params {
+  float* lse;
+  const int32_t* kv_valid;
+  int S_q;
+  int S_kv;
+  int H;
+  int n_pairs;           // query-tile pairs per (b, h)
+  float scale_log2;      // scale * log2(e)
+  int causal;
+  unsigned long long timeout_ns;
+};
+
+}  // namespace
+
+// Set by a bounded wait that gave up; read and cleared by attn_fwd_debug_status.
+__device__ unsigned int g_attn_status = 0;
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+struct WaitCtx {
+  unsigned long long timeout_ns;
+  volatile uint32_t* abort_flag;  // shared memory
+};
+
+// Slow path of a bounded wait.  honour_abort=false is used while draining
+// work already in flight, which must finish even after another role gave up.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
+                                            volatile uint32_t* abort_flag, bool honour_abort) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *abort_flag != 0u) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1u;
+      atomicOr(&g_attn_status, 1u);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, w.timeout_ns, w.abort_flag, true);
+}
+
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, w.timeout_ns, w.abort_flag, false);
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// --- tcgen05 ---------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T-ish per the descriptors; kind::f16 (bf16 in, fp32 acc).
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]; A is read from tensor memory.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+#define ATTN_R32(i) "=r"(r[(i)])
+#define ATTN_OUT32                                                                                          \
+  ATTN_R32(0), ATTN_R32(1), ATTN_R32(2), ATTN_R32(3), ATTN_R32(4), ATTN_R32(5), ATTN_R32(6), ATTN_R32(7),   \
+      ATTN_R32(8), ATTN_R32(9), ATTN_R32(10), ATTN_R32(11), ATTN_R32(12), ATTN_R32(13), ATTN_R32(14),       \
+      ATTN_R32(15), ATTN_R32(16), ATTN_R32(17), ATTN_R32(18), ATTN_R32(19), ATTN_R32(20), ATTN_R32(21),     \
+      ATTN_R32(22), ATTN_R32(23), ATTN_R32(24), ATTN_R32(25), ATTN_R32(26), ATTN_R32(27), ATTN_R32(28),     \
+      ATTN_R32(29), ATTN_R32(30), ATTN_R32(31)
+#define ATTN_I32(i) "r"(r[(i)])
+#define ATTN_IN32                                                                                           \
+  ATTN_I32(0), ATTN_I32(1), ATTN_I32(2), ATTN_I32(3), ATTN_I32(4), ATTN_I32(5), ATTN_I32(6), ATTN_I32(7),   \
+      ATTN_I32(8), ATTN_I32(9), ATTN_I32(10), ATTN_I32(11), ATTN_I32(12), ATTN_I32(13), ATTN_I32(14),       \
+      ATTN_I32(15), ATTN_I32(16), ATTN_I32(17), ATTN_I32(18), ATTN_I32(19), ATTN_I32(20), ATTN_I32(21),     \
+      ATTN_I32(22), ATTN_I32(23), ATTN_I32(24), ATTN_I32(25), ATTN_I32(26), ATTN_I32(27), ATTN_I32(28),     \
+      ATTN_I32(29), ATTN_I32(30), ATTN_I32(31)
+
+// 32 consecutive fp32 columns of this thread's TMEM lane -> r[0..31].
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : ATTN_OUT32
+      : "r"(taddr));
+}
+// r[0..31] -> 32 consecutive columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      ATTN_IN32
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// --- descriptors -----------------------------------------------------------
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N.
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4)                                 // D format: f32
+         | (1u << 7)                               // A format: bf16
+         | (1u << 10)                              // B format: bf16
+         | ((a_mn_major ? 1u : 0u) << 15)          // A major-ness
+         | ((b_mn_major ? 1u : 0u) << 16)          // B major-ness
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, K-major operand: rows of
+// 128 bytes, 8-row groups 1024 bytes apart (the layout TMA writes).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4)  // start address
+         | (static_cast<uint64_t>(1) << 16)             // leading byte offset (unused here)
+         | (static_cast<uint64_t>(1024 >> 4) << 32)     // stride byte offset: 8-row group
+         | (static_cast<uint64_t>(1) << 46)             // descriptor version (sm_100 family)
+         | (static_cast<uint64_t>(2) << 61);            // 128-byte swizzle
+}
+
+// Same, MN-major operand (V as the K x N operand with N = head dim
+// contiguous): 64-element MN blocks `lbo` bytes apart, 8-row K groups 1024 B.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t addr, uint32_t lbo) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// S[tmem] = Q_tile[smem] . K_tile[smem]^T over the head dim (K = D, 16 per MMA).
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>((kk >> 2) * kPanelBytes + (kk & 3) * 32);
+    mma_ss(d_tmem, sdesc_kmajor_sw128(q_smem + off), sdesc_kmajor_sw128(k_smem + off), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O[tmem] (+)= P[tmem] . V_tile[smem] over the keys (K = 128, 16 per MMA).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t idesc,
+                                         bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    mma_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+           sdesc_mnmajor_sw128(v_smem + static_cast<uint32_t>(kk * 16 * 128), kPanelBytes), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Roles
+// ---------------------------------------------------------------------------
+
+template <int D>
+struct Smem {
+  uint32_t base;  // shared address, 1024-aligned
+  __device__ uint32_t q(int t) const { return base + Cfg<D>::kQOff + t * Cfg<D>::kTileBytes; }
+  __device__ uint32_t slot(int s) const { return base + Cfg<D>::kSlotOff + s * Cfg<D>::kTileBytes; }
+  __device__ uint32_t bar(int i) const { return base + Cfg<D>::kBarOff + 8 * i; }
+  __device__ uint32_t bar_q() const { return bar(0); }
+  __device__ uint32_t bar_full(int s) const { return bar(1 + s); }
+  __device__ uint32_t bar_empty(int s) const { return bar(1 + Cfg<D>::kSlots + s); }
+  __device__ uint32_t bar_s(int t) const { return bar(1 + 2 * Cfg<D>::kSlots + t); }
+  __device__ uint32_t bar_p(int t) const { return bar(1 + 2 * Cfg<D>::kSlots + kQTiles + t); }
+  __device__ uint32_t bar_o(int t) const { return bar(1 + 2 * Cfg<D>::kSlots + 2 * kQTiles + t); }
+  __device__ uint32_t bar_drain() const { return bar(1 + 2 * Cfg<D>::kSlots + 3 * kQTiles); }
+};
+
+// TMA producer (one thread).  Item n of the K/V stream is K_{n/2} (n even) or
+// V_{n/2} (n odd) and lives in slot n % kSlots.
+template <int D>
+__device__ void load_role(const Smem<D>& sm, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                          const CUtensorMap* tmV, int bh, int q0, int S_q, int nkv, const WaitCtx& w) {
+  using C = Cfg<D>;
+  tma_prefetch_desc(tmQ);
+  tma_prefetch_desc(tmK);
+  tma_prefetch_desc(tmV);
+  mbar_expect_tx(sm.bar_q(), kQTiles * C::kTileBytes);
+  for (int t = 0; t < kQTiles; ++t) {
+    int y = q0 + t * kBM;
+    if (y >= S_q) y = q0;  // a tile wholly past the end reloads tile 0 (never stored)
+    for (int p = 0; p < C::kPanels; ++p) tma_load_3d(sm.q(t) + p * kPanelBytes, tmQ, sm.bar_q(), p * 64, y, bh);
+  }
+  const int n_items = 2 * nkv;
+  int n = 0;
+  for (; n < n_items; ++n) {
+    const int s = n % C::kSlots;
+    const int round = n / C::kSlots;
+    if (round > 0 && !mbar_wait(sm.bar_empty(s), (round - 1) & 1, w)) break;
+    mbar_expect_tx(sm.bar_full(s), C::kTileBytes);
+    const CUtensorMap* m = (n & 1) ? tmV : tmK;
+    const int y = (n >> 1) * kBN;
+    for (int p = 0; p < C::kPanels; ++p) tma_load_3d(sm.slot(s) + p * kPanelBytes, m, sm.bar_full(s), p * 64, y, bh);
+  }
+  // Every issued copy must land before the CTA can exit (one shared deadline).
+  bool drained = mbar_wait_drain(sm.bar_q(), 0, w);
+  for (int i = (n > C::kSlots ? n - C::kSlots : 0); i < n && drained; ++i) {
+    drained = mbar_wait_drain(sm.bar_full(i % C::kSlots), (i / C::kSlots) & 1, w);
+  }
+}
+
+// MMA issuer (one thread).
+template <int D>
+__device__ void mma_role(const Smem<D>& sm, uint32_t tmem, int nkv, const WaitCtx& w) {
+  using C = Cfg<D>;
+  constexpr uint32_t idesc_s = make_idesc_bf16(kBM, kBN, false, false);
+  constexpr uint32_t idesc_pv = make_idesc_bf16(kBM, D, false, true);
+  const uint32_t tS0 = tmem, tS1 = tmem + kBN;
+  const uint32_t tO0 = tmem + C::kOCol0, tO1 = tmem + C::kOCol0 + D;
+  bool issued = false;
+  bool ok = mbar_wait(sm.bar_q(), 0, w) && mbar_wait(sm.bar_full(0), 0, w);
+  if (ok) {
+    tc_fence_after();
+    issue_qk<D>(tS0, sm.q(0), sm.slot(0), idesc_s);
+    tc_commit(sm.bar_s(0));
+    issue_qk<D>(tS1, sm.q(1), sm.slot(0), idesc_s);
+    tc_commit(sm.bar_s(1));
+    tc_commit(sm.bar_empty(0));
+    issued = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int iv = 2 * j + 1, ik = 2 * j + 2;
+      const int sv = iv % C::kSlots, sk = ik % C::kSlots;
+      const bool has_next = j + 1 < nkv;
+      if (!mbar_wait(sm.bar_full(sv), (iv / C::kSlots) & 1, w)) break;
+      if (has_next && !mbar_wait(sm.bar_full(sk), (ik / C::kSlots) & 1, w)) break;
+      // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T (P0 is read before S0 is overwritten:
+      // MMAs issued by one thread execute in order)
+      if (!mbar_wait(sm.bar_p(0), j & 1, w)) break;
+      tc_fence_after();
+      issue_pv<D>(tO0, tS0, sm.slot(sv), idesc_pv, j > 0);
+      tc_commit(sm.bar_o(0));
+      if (has_next) {
+        issue_qk<D>(tS0, sm.q(0), sm.slot(sk), idesc_s);
+        tc_commit(sm.bar_s(0));
+      }
+      // tile 1
+      if (!mbar_wait(sm.bar_p(1), j & 1, w)) break;
+      tc_fence_after();
+      issue_pv<D>(tO1, tS1, sm.slot(sv), idesc_pv, j > 0);
+      tc_commit(sm.bar_o(1));
+      tc_commit(sm.bar_empty(sv));
+      if (has_next) {
+        issue_qk<D>(tS1, sm.q(1), sm.slot(sk), idesc_s);
+        tc_commit(sm.bar_s(1));
+        tc_commit(sm.bar_empty(sk));
+      }
+    }
+  }
+  if (issued) {  // all MMAs this thread issued are complete before TMEM is freed
+    tc_commit(sm.bar_drain());
+    mbar_wait_drain(sm.bar_drain(), 0, w);
+  }
+}
+
+// Softmax + epilogue for query tile t (128 threads, one query row each).
+template <int D>
+__device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const CUtensorMap* tmO, const Params& p,
+                             int bh, int q0, int nk_pad, int nkv, const WaitCtx& w) {
+  using C = Cfg<D>;
+  const int r = static_cast<int>(threadIdx.x) - kBM * (1 + t);  // row in tile == TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_off + t * kBN;
+  const uint32_t tO = tmem + lane_off + C::kOCol0 + t * D;
+  const int qs = q0 + t * kBM;
+  const int row = qs + r;
+  int lim = nk_pad;  // keys j < lim are allowed for this row
+  if (p.causal) lim = min(lim, row + 1);
+  const float c = p.scale_log2;
+
+  float m_c = -INFINITY;  // running max, in scaled log2 units, as used for P
+  float l = 0.f;          // running sum of P relative to m_c
+  bool ok = true;
+  for (int j = 0; j < nkv; ++j) {
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_s(t), j & 1, w));
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t sr[kBN];
+    tmem_ld32(tS + 0, sr + 0);
+    tmem_ld32(tS + 32, sr + 32);
+    tmem_ld32(tS + 64, sr + 64);
+    tmem_ld32(tS + 96, sr + 96);
+    tmem_wait_ld();
+    float s[kBN];
+#pragma unroll
+    for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sr[i]);
+
+    const int kbase = j * kBN;
+    if (kbase + kBN > nk_pad || (p.causal && kbase + kBN - 1 > qs)) {
+      const int lj = lim - kbase;
+#pragma unroll
+      for (int i = 0; i < kBN; ++i) s[i] = (i < lj) ? s[i] : -INFINITY;
+    }
+    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+    for (int i = 4; i < kBN; i += 4) {
+      mx0 = fmaxf(mx0, s[i]);
+      mx1 = fmaxf(mx1, s[i + 1]);
+      mx2 = fmaxf(mx2, s[i + 2]);
+      mx3 = fmaxf(mx3, s[i + 3]);
+    }
+    const float new_mc = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+    float alpha = 1.f;
+    bool rescale_o = false;
+    if (new_mc > m_c + kRescaleLog2) {  // also taken on the first tile (m_c = -inf)
+      alpha = ex2_approx(m_c - new_mc);
+      rescale_o = j > 0;  // O holds data only after the first P.V
+      m_c = new_mc;
+    }
+    const float mc = (m_c == -INFINITY) ? 0.f : m_c;
+
+    uint32_t pk[kBN / 2];
+    float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kBN / 2; ++i) {
+      const float a = ex2_approx(fmaf(s[2 * i], c, -mc));
+      const float b = ex2_approx(fmaf(s[2 * i + 1], c, -mc));
+      sum0 += a;
+      sum1 += b;
+      pk[i] = pack_bf16x2(a, b);
+    }
+    l = l * alpha + (sum0 + sum1);
+    tmem_st32(tS + 0, pk + 0);
+    tmem_st32(tS + 32, pk + 32);
+    tmem_wait_st();
+
+    // Lazy correction: O is rescaled only when some row's max grew by > 2^8.
+    if (__any_sync(0xffffffffu, rescale_o)) {
+      ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (j - 1) & 1, w));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + cc, o);
+        }
+        tmem_wait_st();
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(sm.bar_p(t));
+    if (!ok) break;
+  }
+
+  // Epilogue: O / l -> bf16 -> swizzled smem (reusing this tile's Q buffer) ->
+  // TMA store; LSE = (m + log2 l) ln 2, one coalesced fp32 store per row.
+  float inv_l = 0.f, lse = -INFINITY;
+  if (l > 0.f) {
+    inv_l = 1.f / l;
+    lse = (m_c + log2f(l)) * kLn2;
+  }
+  bool have_o = ok && nkv > 0;
+  if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (nkv - 1) & 1, w));
+  if (have_o) tc_fence_after();
+  const uint32_t stage = sm.q(t);
+#pragma unroll 1
+  for (int cc = 0; cc < D; cc += 32) {
+    uint32_t o[32];
+    if (have_o) {
+      tmem_ld32(tO + cc, o);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = 0u;
+    }
+    uint32_t wv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      wv[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+    const uint32_t panel = stage + static_cast<uint32_t>((cc >> 6) * kPanelBytes) + static_cast<uint32_t>(r * 128);
+    const int chunk0 = (cc & 63) >> 3;  // 16-byte chunk of column cc within the 128-byte row
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t addr = panel + static_cast<uint32_t>(((chunk0 + u) ^ (r & 7)) << 4);
+      st_shared_v4(addr, wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
+    }
+  }
+  fence_proxy_async_smem();
+  named_bar_sync(1 + t, kBM);
+  if (r == 0 && qs < p.S_q) {
+    for (int pn = 0; pn < C::kPanels; ++pn) tma_store_3d(tmO, stage + pn * kPanelBytes, pn * 64, qs, bh);
+    bulk_commit();
+    bulk_wait_read0();
+  }
+  if (row < p.S_q) p.lse[static_cast<int64_t>(bh) * p.S_q + row] = lse;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const Smem<D> sm{base};
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
+
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int bh = static_cast<int>(blockIdx.x) / p.n_pairs;
+  const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x) % p.n_pairs;  // heaviest first
+  const int q0 = pair * kRowsPerCta;
+  const int b = bh / p.H;
+
+  int nk_pad = p.S_kv;  // keys allowed by padding
+  if (p.kv_valid != nullptr) nk_pad = min(max(p.kv_valid[b], 0), p.S_kv);
+  int nk = nk_pad;  // keys any row of this CTA can see
+  if (p.causal) nk = min(nk, min(q0 + kRowsPerCta, p.S_q));
+  const int nkv = (nk + kBN - 1) / kBN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(sm.bar_q(), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(sm.bar_full(s), 1);
+      mbar_init(sm.bar_empty(s), 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(sm.bar_s(t), 1);
+      mbar_init(sm.bar_p(t), kBM);
+      mbar_init(sm.bar_o(t), 1);
+    }
+    mbar_init(sm.bar_drain(), 1);
+    misc[1] = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(base + C::kMiscOff, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const WaitCtx w{p.timeout_ns, misc + 1};
+
+  if (warp == 0) {
+    if (lane == 0 && nkv > 0) load_role<D>(sm, &tmQ, &tmK, &tmV, bh, q0, p.S_q, nkv, w);
+  } else if (warp == 1) {
+    if (lane == 0 && nkv > 0) mma_role<D>(sm, tmem, nkv, w);
+  } else if (warp >= 4) {
+    softmax_role<D>(sm, (warp - 4) >> 2, tmem, &tmO, p, bh, q0, nk_pad, nkv, w);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// S_kv == 0: every row has no allowed key -> O = 0, LSE = -inf.
+__global__ void attn_fill_empty(uint16_t* o, float* lse, int64_t rows, int D) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    for (int d = 0; d < D; ++d) o[i * D + d] = 0;
+    lse[i] = -INFINITY;
+  }
+}
+
+// Waits on a barrier nothing completes; the bounded wait must give up.
+__global__ void attn_watchdog_kernel(unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const WaitCtx w{timeout_ns, &abort_flag};
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, w);
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  });
+  return g_encode != nullptr;
+}
+
+// [BH][S][D] bf16 as a 3-D tensor map with 64 x 128 x 1 boxes, 128-byte swizzle.
+bool encode_3d(CUtensorMap* m, const void* ptr, int D, int S, int64_t BH) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, 2 unsupported
+
+// Checks the device is sm_103 and sets the kernels' shared-memory limits once.
+attn_status_t prepare_device(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  const int st = g_dev_state[dev].load(std::memory_order_acquire);
+  if (st == 1) return ATTN_OK;
+  if (st == 2) return ATTN_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ATTN_ERR_DEVICE;
+  if (major != 10 || minor != 3) {
+    g_dev_state[dev].store(2, std::memory_order_release);
+    return ATTN_ERR_UNSUPPORTED;
+  }
+  if (cudaFuncSetAttribute(attn_fwd_sm103a<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<64>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128>::kSmemBytes) != cudaSuccess)
+    return ATTN_ERR_DEVICE;
+  g_dev_state[dev].store(1, std::memory_order_release);
+  return ATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+template <int D>
+attn_status_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S_q,
+                     int S_kv, float scale, int causal, const int32_t* kv_valid_len, cudaStream_t stream) {
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  CUtensorMap tq, tk, tv, to;
+  if (!encode_3d(&tq, q, D, S_q, BH) || !encode_3d(&tk, k, D, S_kv, BH) || !encode_3d(&tv, v, D, S_kv, BH) ||
+      !encode_3d(&to, o, D, S_q, BH))
+    return ATTN_ERR_LAUNCH;
+  Params prm;
+  prm.lse = lse;
+  prm.kv_valid = kv_valid_len;
+  prm.S_q = S_q;
+  prm.S_kv = S_kv;
+  prm.H = H;
+  prm.n_pairs = (S_q + kRowsPerCta - 1) / kRowsPerCta;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  prm.causal = causal;
+  prm.timeout_ns = kDefaultTimeoutNs;
+  const int64_t grid = BH * prm.n_pairs;
+  attn_fwd_sm103a<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd_abi_version(void) { return 1; }
+
+const char* attn_status_str(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case ATTN_ERR_ALIGNMENT: return "misaligned pointer";
+    case ATTN_ERR_LAUNCH: return "kernel launch failed";
+    case ATTN_ERR_TIMEOUT: return "in-kernel wait timed out";
+    case ATTN_ERR_DEVICE: return "CUDA device error";
+  }
+  return "unknown status";
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S_q,
+                       int S_kv, int D, float scale, int causal, const int32_t* kv_valid_len, void* stream) {
+  if (B < 1 || H < 1 || S_q < 0 || S_kv < 0) return ATTN_ERR_INVALID_ARG;
+  // a buffer may be null only when its extent is zero (empty tensors)
+  if (S_q > 0 && (q == nullptr || o == nullptr || lse == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (S_q > 0 && S_kv > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(kv_valid_len, 4))
+    return ATTN_ERR_ALIGNMENT;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const int64_t n_pairs = (static_cast<int64_t>(S_q) + kRowsPerCta - 1) / kRowsPerCta;
+  if (BH * n_pairs > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  if (S_q == 0) return ATTN_OK;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+  const attn_status_t ps = prepare_device(dev);
+  if (ps != ATTN_OK) return ps;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  if (S_kv == 0) {
+    const int64_t rows = BH * S_q;
+    const int64_t blocks = std::min<int64_t>((rows + 255) / 256, 4096);
+    attn_fill_empty<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<uint16_t*>(o), lse, rows, D);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  }
+  if (!get_encoder()) return ATTN_ERR_DEVICE;
+  if (D == 64) return launch<64>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, st);
+  return launch<128>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, st);
+}
+
+attn_status_t attn_fwd_debug_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_DEVICE;
+  unsigned int word = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_attn_status, sizeof word) != cudaSuccess) return ATTN_ERR_DEVICE;
+  if (word != 0u && cudaMemcpyToSymbol(g_attn_status, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_DEVICE;
+  return word != 0u ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+attn_status_t attn_watchdog_selftest(uint64_t timeout_ns, void* stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 10000000000ull) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  attn_watchdog_kernel<<<1, 32, 0, st>>>(timeout_ns);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return attn_fwd_debug_status(stream);
+}
+
+}  // extern "C"

@@ -151,3 +151,71 @@ def sample_rows(seed: int, S: int, n: int, must_include=()) -> np.ndarray:
         if i >= S:
             break
     return np.array(sorted(chosen[:n]), dtype=np.int64)
+
+
+# --- the same generator on a torch device (bench inputs at full size) --------
+
+def _to_i64(x: int) -> int:
+    x &= (1 << 64) - 1
+    return x - (1 << 64) if x >= (1 << 63) else x
+
+
+def _lsr_t(z, k: int):
+    """Logical right shift of an int64 tensor viewed as uint64."""
+    return (z >> k) & ((1 << (64 - k)) - 1)
+
+
+def _mix64_t(z):
+    z = (z ^ _lsr_t(z, 30)) * _to_i64(0xBF58476D1CE4E5B9)
+    z = (z ^ _lsr_t(z, 27)) * _to_i64(0x94D049BB133111EB)
+    return z ^ _lsr_t(z, 31)
+
+
+def _mix64_int(z: int) -> int:
+    m = (1 << 64) - 1
+    z &= m
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & m
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & m
+    return z ^ (z >> 31)
+
+
+def normal_bf16_torch(seed: int, tensor_id: int, count: int, multiplier: float = 1.0,
+                      device="cuda", chunk: int = 1 << 25):
+    """Same definition as ``normal_bf16`` computed with torch on ``device``.
+
+    Returns a bfloat16 tensor of ``count`` elements.  The float64 log, sqrt,
+    cos and sin of the device may differ from the host's in the last place,
+    which can move a value by one bf16 step in rare cases; parity tests
+    therefore draw on the host, and this path serves the benchmark.
+    """
+    import torch
+
+    if multiplier != 1.0 and math.frexp(multiplier)[0] != 0.5:
+        raise ValueError("multiplier must be a power of two")
+    s0 = _mix64_int(seed * 0x9E3779B97F4A7C15 + tensor_id)
+    gamma = _to_i64(0x9E3779B97F4A7C15)
+    out = torch.empty(count, dtype=torch.bfloat16, device=device)
+    for lo in range(0, count, chunk):
+        n = min(chunk, count - lo)
+        npairs = (n + 1) // 2
+        idx = torch.arange(lo + 1, lo + 2 * npairs + 1, dtype=torch.int64, device=device)
+        w = _mix64_t(idx * gamma + _to_i64(s0))
+        u = (_lsr_t(w, 11).to(torch.float64) + 0.5) * (2.0 ** -53)
+        u1, u2 = u[0::2], u[1::2]
+        r = torch.sqrt(-2.0 * torch.log(u1))
+        th = (2.0 * math.pi) * u2
+        z = torch.stack([r * torch.cos(th), r * torch.sin(th)], dim=1).reshape(-1)[:n]
+        x = z.to(torch.float32).to(torch.bfloat16)
+        if multiplier != 1.0:
+            x = x * multiplier
+        out[lo:lo + n] = x
+    return out
+
+
+def qkv_bf16_torch(seed: int, B: int, H: int, S_q: int, S_kv: int, D: int,
+                   q_mult: float = 1.0, k_mult: float = 1.0, device="cuda"):
+    """Q, K, V of one workload as bf16 tensors [B,H,S,D] on ``device``."""
+    q = normal_bf16_torch(seed, TID_Q, B * H * S_q * D, q_mult, device).view(B, H, S_q, D)
+    k = normal_bf16_torch(seed, TID_K, B * H * S_kv * D, k_mult, device).view(B, H, S_kv, D)
+    v = normal_bf16_torch(seed, TID_V, B * H * S_kv * D, 1.0, device).view(B, H, S_kv, D)
+    return q, k, v

@@ -1,0 +1,213 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on GB300.
+
+The five workloads of the target (small, 1k, 4k causal, 8k padded, 32k causal)
+plus edge cases: ragged tails, S_q != S_kv, key-padding lengths around tile
+boundaries, empty inputs, peaked softmax, determinism, no device allocation,
+and the watchdog's failure path.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+
+import seeded_inputs as si
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import io_aware_attention_fwd_gb300 as attn
+    attn.build()
+    return torch.device("cuda:0")
+
+
+def qkv(seed, B, H, S_q, S_kv, D, q_mult=1.0, k_mult=1.0):
+    return si.qkv_bf16(seed, B, H, S_q, S_kv, D, q_mult, k_mult)
+
+
+# --- the five workloads --------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_c1_small_all_rows(dev, causal):
+    q, k, v = qkv(1, 1, 2, 128, 128, 64)
+    parity.check_against_oracle(q, k, v, 1 / 8, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("peaked", [False, True])
+def test_c2_1k_all_rows(dev, causal, peaked):
+    seed, mult = (3, 8.0) if peaked else (2, 1.0)
+    q, k, v = qkv(seed, 4, 16, 1024, 1024, 64, q_mult=mult)
+    parity.check_against_oracle(q, k, v, 1 / 8, causal)
+
+
+@pytest.fixture(scope="module")
+def c3(dev):
+    q, k, v = qkv(4, 1, 32, 4096, 4096, 128)
+    return q, k, v, tuple(parity.to_device(x, dev) for x in (q, k, v))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_c3_4k_d128(c3, causal):
+    q, k, v, t = c3
+    heads = [(0, h) for h in si.sample_rows(40, 32, 4)]
+    rows = parity.sampled_rows(4, 1, 32, 4096, 256, full_heads=heads, must_include=[0, 4095])
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(128), causal, rows=rows, tensors=t)
+
+
+def test_c4_8k_padded(dev):
+    q, k, v = qkv(5, 2, 32, 8192, 8192, 128)
+    rows = parity.sampled_rows(5, 2, 32, 8192, 256, must_include=[0, 4999, 5000, 8191])
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(128), False, kv_valid_len=[8192, 5000], rows=rows)
+
+
+@pytest.fixture(scope="module")
+def c5(dev):
+    S = 32768
+    q, k, v = qkv(6, 1, 32, S, S, 128, q_mult=2.0, k_mult=2.0)
+    return q, k, v, tuple(parity.to_device(x, dev) for x in (q, k, v))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_c5_32k(c5, causal):
+    q, k, v, t = c5
+    S = 32768
+    rows = parity.sampled_rows(6, 1, 32, S, 128, must_include=[0, 1, 127, 128, S // 2, S - 1])
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(128), causal, rows=rows, tensors=t)
+
+
+# --- edge cases ----------------------------------------------------------------
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("S", [1, 2, 127, 129, 200, 255, 257, 383, 640])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths(dev, D, S, causal):
+    q, k, v = qkv(100 + S, 1, 3, S, S, D)
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(D), causal)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("S_q,S_kv", [(100, 300), (300, 100), (1, 513), (513, 1), (256, 640)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_unequal_query_and_key_lengths(dev, D, S_q, S_kv, causal):
+    q, k, v = qkv(200 + S_q + S_kv, 2, 2, S_q, S_kv, D)
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(D), causal)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_padding_around_tile_edges(dev, D, causal):
+    valid = [0, 1, 127, 128, 129, 300, 500]
+    q, k, v = qkv(300, len(valid), 2, 300, 300, D)
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(D), causal, kv_valid_len=valid)
+
+
+def test_padding_length_out_of_range_is_clamped(dev):
+    q, k, v = qkv(301, 3, 1, 64, 200, 64)
+    o1, l1 = parity.run_cuda(q, k, v, 0.125, False, kv_valid_len=[-7, 10**6, 200])
+    o2, l2 = parity.run_cuda(q, k, v, 0.125, False, kv_valid_len=[0, 200, 200])
+    import torch
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_peaked_softmax_rescaling(dev, D):
+    # Q x 8 makes every row nearly one-hot; Q, K x 2 stresses the max-growth path.
+    q, k, v = qkv(400, 2, 4, 700, 700, D, q_mult=8.0)
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(D), False)
+    q, k, v = qkv(401, 2, 4, 700, 700, D, q_mult=2.0, k_mult=2.0)
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(D), True)
+
+
+def test_increasing_scores_force_every_rescale(dev):
+    # Scores grow with the key index, so the running max rises on every tile.
+    S, D = 1024, 64
+    q = np.zeros((1, 1, S, D), np.uint16)
+    q[..., 0] = 0x3F80  # 1.0
+    keys = si.f32_to_bf16_bits(np.linspace(0.0, 60.0, S, dtype=np.float32))
+    k = np.zeros((1, 1, S, D), np.uint16)
+    k[0, 0, :, 0] = keys
+    v = si.normal_bf16(402, si.TID_V, S * D).reshape(1, 1, S, D)
+    for causal in (False, True):
+        parity.check_against_oracle(q, k, v, 1.0, causal)
+
+
+def test_large_head_count_small_sequence(dev):
+    q, k, v = qkv(500, 8, 64, 64, 64, 64)
+    parity.check_against_oracle(q, k, v, 0.125, True)
+
+
+def test_empty_keys_and_queries(dev):
+    import torch
+    import io_aware_attention_fwd_gb300 as attn
+    q, _, _ = qkv(600, 2, 2, 50, 1, 64)
+    e = np.zeros((2, 2, 0, 64), np.uint16)
+    parity.check_against_oracle(q, e, e, 0.125, False)
+    # S_q == 0: nothing is written
+    z = torch.zeros((1, 1, 0, 64), dtype=torch.bfloat16, device=dev)
+    kk = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((1,), dtype=torch.float32, device=dev)
+    attn.attn_fwd(kk, kk, kk, kk, lse, 1, 1, 0, 8, 64, 0.125, False)
+    torch.cuda.synchronize()
+
+
+def test_deterministic(dev):
+    q, k, v = qkv(700, 2, 8, 1000, 1000, 128)
+    t = tuple(parity.to_device(x, dev) for x in (q, k, v))
+    o1, l1 = parity.run_cuda(q, k, v, 0.1, True, tensors=t)
+    o2, l2 = parity.run_cuda(q, k, v, 0.1, True, tensors=t)
+    import torch
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_side_stream_and_api_wrapper(dev):
+    import torch
+    import io_aware_attention_fwd_gb300 as attn
+    q, k, v = qkv(800, 1, 4, 300, 300, 128)
+    t = [parity.to_device(x, dev) for x in (q, k, v)]
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        o, lse = attn.attention_forward(*t, causal=True)
+    s.synchronize()
+    o_gpu, l_gpu = parity.gather_rows(o, lse)
+    import oracle
+    o_ref, l_ref = oracle.attention_f64(q, k, v, 1 / math.sqrt(128), True)
+    parity.compare(o_gpu, l_gpu, o_ref, l_ref)
+
+
+def test_library_allocates_no_device_memory(dev):
+    import torch
+    import io_aware_attention_fwd_gb300 as attn
+    q, k, v = qkv(900, 1, 8, 4096, 4096, 128)
+    t = [parity.to_device(x, dev) for x in (q, k, v)]
+    o = torch.empty_like(t[0])
+    lse = torch.empty((1, 8, 4096), dtype=torch.float32, device=dev)
+    attn.attn_fwd(*t, o, lse, 1, 8, 4096, 4096, 128, 0.1, True)  # first call loads the module
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(dev)
+    for causal in (False, True):
+        attn.attn_fwd(*t, o, lse, 1, 8, 4096, 4096, 128, 0.1, causal)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert free1 == free0
+    # 8 heads x 4096^2 fp32 scores would need 512 MiB; no such buffer exists
+    assert torch.cuda.memory_allocated(dev) < 64 * 2**20 + 4 * t[0].numel() * 2
+
+
+def test_watchdog_gives_up_and_context_survives(dev):
+    import torch
+    import io_aware_attention_fwd_gb300 as attn
+    assert attn.attn_fwd_debug_status() == attn.ATTN_OK
+    assert attn.attn_watchdog_selftest(2_000_000) == attn.ATTN_ERR_TIMEOUT  # 2 ms limit
+    assert attn.attn_fwd_debug_status() == attn.ATTN_OK  # the word was cleared
+    # the context is still usable
+    q, k, v = qkv(1000, 1, 2, 256, 256, 64)
+    parity.check_against_oracle(q, k, v, 0.125, True)
+    torch.cuda.synchronize()

@@ -60,3 +60,16 @@ def test_sample_rows_distinct_and_required():
     assert np.array_equal(r, si.sample_rows(6, 32768, 128, must_include=[0, 1, 16384, 32767]))
     small = si.sample_rows(1, 10, 50)
     assert small.tolist() == list(range(10))
+
+
+def test_torch_generator_matches_host_generator():
+    torch = __import__("pytest").importorskip("torch")
+    n = 200_001
+    host = si.normal_bf16(3, si.TID_K, n, multiplier=2.0)
+    dev = si.normal_bf16_torch(3, si.TID_K, n, multiplier=2.0, device="cpu", chunk=65536)
+    dev_bits = dev.view(torch.int16).numpy().view(np.uint16)
+    same = host == dev_bits
+    assert same.mean() > 0.9999
+    # any difference is a single bf16 step
+    diff = np.abs(host.astype(np.int32) - dev_bits.astype(np.int32))
+    assert diff.max() <= 1
