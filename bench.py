@@ -89,6 +89,24 @@ def alg_bytes(w, causal):
     return H * (2 * S * D * 2 * B + 2 * kv * D * 2 + S * 4 * B)
 
 
+def aggregate_ranks(flops_step, t_step_ms, t_e2e_ms, dist=None, device="cpu"):
+    """Whole-job numbers over all ranks: (value, e2e value, max step ms, max e2e ms).
+
+    Every rank processes its own replica; the job's work is the sum of the
+    ranks' FLOPs and its time is the slowest rank's, so value = sum / max.
+    """
+    if dist is None:
+        t_max, t_e2e_max, total = t_step_ms, t_e2e_ms, flops_step
+    else:
+        import torch
+        t = torch.tensor([t_step_ms, t_e2e_ms], dtype=torch.float64, device=device)
+        f = torch.tensor([float(flops_step)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(f, op=dist.ReduceOp.SUM)
+        t_max, t_e2e_max, total = float(t[0]), float(t[1]), float(f[0])
+    return total / (t_max * 1e-3) / 1e12, total / (t_e2e_max * 1e-3) / 1e12, t_max, t_e2e_max
+
+
 def load_peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -236,7 +254,7 @@ def run_reference(args, w, rank):
 
     q, k, v = si.qkv_bf16(w["seed"], w["B"], w["H"], w["S"], w["S"], w["D"],
                           w.get("q_mult", 1.0), w.get("k_mult", 1.0))
-    per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    per_step = max(0.2, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample(w, q, k, v, per_step, w["modes"])
     vals, secs, rows, threads = [], 0.0, 0, 1
@@ -270,6 +288,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-settle", action="store_true",
+                    help="skip the 1 s busy loop before timing (for profiler runs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target oracle time for the cpu_baseline sample (0 disables)")
     args = ap.parse_args()
@@ -338,7 +358,7 @@ def main():
     sampler = ClockSampler(local_rank)
     sampler.start()
     # keep the GPU busy for ~1 s before timing so clock samples see load
-    t_end = time.perf_counter() + 1.0
+    t_end = time.perf_counter() + (0.0 if args.no_settle else 1.0)
     while time.perf_counter() < t_end:
         for causal in modes:
             launch(causal)
@@ -377,14 +397,8 @@ def main():
         raise RuntimeError(f"device status after timing: {attn.attn_status_str(st)}")
 
     flops_step = sum(alg_flops(w, c) for c in modes)
-    t_step = sum(step_ms) / len(step_ms)
-    t_e2e = sum(e2e_ms) / len(e2e_ms)
-    if dist is not None:
-        t = torch.tensor([t_step, t_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, t_e2e = float(t[0]), float(t[1])
-    value = world * flops_step / (t_step * 1e-3) / 1e12
-    e2e_value = world * flops_step / (t_e2e * 1e-3) / 1e12
+    value, e2e_value, t_step, t_e2e = aggregate_ranks(
+        flops_step, sum(step_ms) / len(step_ms), sum(e2e_ms) / len(e2e_ms), dist, dev)
 
     # roofline of the attention kernel: every launch in the step is attn_fwd_sm103a<D>
     mean_launch_ms = sum(sum(x) for x in launch_ms) / (args.steps * n_l)

@@ -1,0 +1,83 @@
+"""Host logic of bench.py: FLOP accounting, rank aggregation over gloo
+(world size 2, CPU), and the reference arm under torchrun."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+from pathlib import Path
+
+import pytest
+
+import bench
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+def test_flop_accounting_matches_closed_forms():
+    w = bench.WORKLOADS["b1_h32_s4096_d128"]
+    assert bench.alg_flops(w, True) == 4 * 32 * 128 * 4096 * 4097 // 2
+    assert bench.alg_flops(w, False) == 4 * 32 * 128 * 4096 * 4096
+    w = bench.WORKLOADS["b2_h32_s8192_d128_padded"]
+    assert bench.alg_flops(w, False) == 4 * 32 * 128 * 8192 * (8192 + 5000)
+    # causal with padding: row i sees min(valid, i + 1) keys
+    assert bench.allowed_pairs(1, 1, 6, 6, True, [3]) == 1 + 2 + 3 + 3 + 3 + 3
+    assert bench.allowed_pairs(1, 1, 4, 9, True) == 1 + 2 + 3 + 4
+    assert bench.allowed_pairs(1, 1, 9, 4, True) == 1 + 2 + 3 + 4 * 6
+    assert bench.allowed_pairs(2, 1, 5, 5, False, [0, 2]) == 0 + 10
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # rank r: 1e12 * (r + 1) FLOPs per step in (10 + r) ms, e2e (20 + 5 r) ms
+    res = bench.aggregate_ranks(1e12 * (rank + 1), 10.0 + rank, 20.0 + 5 * rank, dist, "cpu")
+    out.put((rank, res))
+    dist.destroy_process_group()
+
+
+def test_rank_aggregation_gloo_world2():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in (0, 1):
+        value, e2e, t, te = got[r]
+        assert t == 11.0 and te == 25.0                    # slowest rank
+        assert value == pytest.approx(3e12 / 11e-3 / 1e12)  # summed work / max time
+        assert e2e == pytest.approx(3e12 / 25e-3 / 1e12)
+
+
+def test_single_rank_aggregation():
+    value, e2e, t, te = bench.aggregate_ranks(2e12, 4.0, 8.0)
+    assert (value, e2e, t, te) == (500.0, 250.0, 4.0, 8.0)
+
+
+def test_reference_arm_under_torchrun_world2():
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), str(ROOT / "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-seconds", "0.3"]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1  # rank 0 alone prints
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["config"]["workload"] == bench.DEFAULT_WORKLOAD
