@@ -12,25 +12,31 @@
 //     memory (TMEM) and never sends it to HBM.
 //   * "Flash attention" glossary (news.hamidun.com), second paragraph: tiles
 //     that fit on-chip, an incremental numerically stable softmax,
-//     parallelism across the sequence (the grid runs over query tiles), fewer
-//     non-matmul operations (exp2 with the scale folded in, the 1/l division
-//     deferred to the epilogue, lazy rescaling of O), and warp specialisation.
+//     parallelism across the sequence (the work units are query tiles), fewer
+//     non-matmul operations (exp2 with the scale folded in, packed fp32x2
+//     arithmetic, the 1/l division deferred to the epilogue, lazy rescaling
+//     of O), and warp specialisation.
 //   * "PyTorch attention backends" story (hyper.ai), masked_fill sentences:
 //     a masked key scores -inf.  Here the causal and key-padding predicates
 //     are evaluated from indices in registers; no mask tensor exists.
 //
-// One CTA computes two 128-row query tiles of one (batch, head) against all
-// of that head's allowed keys.  Warp roles (384 threads):
-//   warp 0       TMA producer: Q tiles once, then K/V tiles into a ring of
-//                shared-memory slots guarded by mbarriers.
+// Persistent kernel: one CTA per SM walks a static list of work units.  A
+// unit is two 128-row query tiles of one (batch, head) against that head's
+// allowed keys.  Warp roles (384 threads):
+//   warp 0       TMA producer: per unit the two Q tiles, then K/V tiles into a
+//                ring of shared-memory slots guarded by mbarriers.  The ring
+//                runs on across units, so the next unit's Q and first K/V
+//                tiles load while the current unit finishes.
 //   warp 1       tcgen05.mma issuer (one thread): S_t = Q_t K_j^T into TMEM,
 //                then O_t += P_t V_j with P_t read from TMEM.
 //   warps 4-7    softmax for query tile 0; warps 8-11 for query tile 1.  One
 //                thread owns one query row (one TMEM lane): it reads its S
 //                row, masks, updates the running max and sum, writes P (bf16)
-//                back over S, rescales O lazily, and runs the epilogue.
+//                back over S, rescales O lazily, and writes O and LSE at the
+//                end of the unit straight from registers to global memory.
 // While one softmax warpgroup works on its tile, the tensor core runs the
-// other tile's MMAs, so exp2 work and MMAs overlap.
+// other tile's MMAs, so exp2 work and MMAs overlap; across units, the next
+// unit's S MMAs run while the softmax warpgroups drain the previous O.
 //
 // Every wait on a barrier is bounded by a %globaltimer deadline.  A wait that
 // gives up sets a shared abort flag and a device status word, and every role
@@ -41,6 +47,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -53,8 +60,8 @@ namespace {
 
 constexpr int kBM = 128;              // query rows per softmax tile (TMEM lanes)
 constexpr int kBN = 128;              // keys per kv tile
-constexpr int kQTiles = 2;            // query tiles per CTA
-constexpr int kRowsPerCta = kBM * kQTiles;
+constexpr int kQTiles = 2;            // query tiles per work unit
+constexpr int kRowsPerUnit = kBM * kQTiles;
 constexpr int kThreads = 384;         // warps 0-3: roles, 4-7 / 8-11: softmax
 constexpr uint32_t kTmemCols = 512;   // S0 | S1 | O0 | O1
 constexpr int kPanelBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
@@ -67,24 +74,29 @@ struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kPanels = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;  // one [128 x D] bf16 tile
-  static constexpr int kSlots = (D == 128) ? 4 : 8;
+  static constexpr int kSlots = (D == 128) ? 5 : 12;
   static constexpr int kQOff = 0;
   static constexpr int kSlotOff = kQTiles * kTileBytes;
   static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
-  // barriers: q_full | full[kSlots] | empty[kSlots] | s_full[2] | p_full[2] | o_done[2] | drain
-  static constexpr int kNumBars = 1 + 2 * kSlots + 3 * kQTiles + 1;
+  // barriers: q_full | q_free[2] | full[kSlots] | empty[kSlots] | s_full[2] | p_full[2] |
+  //           o_done[2] | drain
+  static constexpr int kNumBars = 1 + kQTiles + 2 * kSlots + 3 * kQTiles + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] tmem base, [1] abort flag
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024 B alignment
   static constexpr int kOCol0 = kQTiles * kBN;             // first O column in TMEM
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 struct Params {
-  float* lse;
+  uint16_t* o;           // bf16 bits [BH][S_q][D]
+  float* lse;            // [BH][S_q]
   const int32_t* kv_valid;
   int S_q;
   int S_kv;
   int H;
+  int BH;
   int n_pairs;           // query-tile pairs per (b, h)
+  int n_units;           // BH * n_pairs
   float scale_log2;      // scale * log2(e)
   int causal;
   unsigned long long timeout_ns;
@@ -184,30 +196,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(src), "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
 // --- tcgen05 ---------------------------------------------------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -228,31 +216,49 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T-ish per the descriptors; kind::f16 (bf16 in, fp32 acc).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// One lane of a converged warp (elect.sync); the MMA warp runs warp-wide so
+// its addresses and descriptors stay warp-uniform, and only the elected lane
+// issues tcgen05.mma / tcgen05.commit.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t e;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e;
+}
+
+// Arrive once on `bar` when every tcgen05 op the calling lane issued so far is
+// done; only lanes with `pred` set commit.
+__device__ __forceinline__ void tc_commit_if(uint32_t pred, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(pred)
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]; A is read from tensor memory.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// The same MMAs as below, issued only when `pred` is set (the elected lane).
+__device__ __forceinline__ void mma_ss_if(uint32_t pred, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_if(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
       : "memory");
 }
 
@@ -336,29 +342,61 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t addr, uint32_t 
 }
 
 // S[tmem] = Q_tile[smem] . K_tile[smem]^T over the head dim (K = D, 16 per MMA).
+// qd/kd are the tiles' base descriptors; a step of k elements within a
+// 128-byte swizzle row adds 32 bytes (2 in the 16-byte address field), and
+// the next 64-column panel adds kPanelBytes.  Addresses stay below 256 KB, so
+// the 14-bit field never carries.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem, uint32_t idesc) {
+__device__ __forceinline__ void issue_qk(uint32_t pred, uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc) {
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = static_cast<uint32_t>((kk >> 2) * kPanelBytes + (kk & 3) * 32);
-    mma_ss(d_tmem, sdesc_kmajor_sw128(q_smem + off), sdesc_kmajor_sw128(k_smem + off), idesc, kk > 0 ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
+    mma_ss_if(pred, d_tmem, qd + off, kd + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// O[tmem] (+)= P[tmem] . V_tile[smem] over the keys (K = 128, 16 per MMA).
+// O[tmem] (+)= P[tmem] . V_tile[smem] over the keys (K = 128, 16 per MMA); a
+// step of 16 keys is 16 rows of 128 bytes in the MN-major V layout.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t idesc,
+__device__ __forceinline__ void issue_pv(uint32_t pred, uint32_t d_tmem, uint32_t p_tmem, uint64_t vd, uint32_t idesc,
                                          bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
-    mma_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
-           sdesc_mnmajor_sw128(v_smem + static_cast<uint32_t>(kk * 16 * 128), kPanelBytes), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts_if(pred, d_tmem, p_tmem + static_cast<uint32_t>(kk * 8), vd + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+              idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
+// --- small arithmetic helpers ----------------------------------------------
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// two fp32 products in one instruction
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// three-input maximum
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
-// Roles
+// Work units and shared-memory map
 // ---------------------------------------------------------------------------
 
 template <int D>
@@ -368,241 +406,359 @@ struct Smem {
   __device__ uint32_t slot(int s) const { return base + Cfg<D>::kSlotOff + s * Cfg<D>::kTileBytes; }
   __device__ uint32_t bar(int i) const { return base + Cfg<D>::kBarOff + 8 * i; }
   __device__ uint32_t bar_q() const { return bar(0); }
-  __device__ uint32_t bar_full(int s) const { return bar(1 + s); }
-  __device__ uint32_t bar_empty(int s) const { return bar(1 + Cfg<D>::kSlots + s); }
-  __device__ uint32_t bar_s(int t) const { return bar(1 + 2 * Cfg<D>::kSlots + t); }
-  __device__ uint32_t bar_p(int t) const { return bar(1 + 2 * Cfg<D>::kSlots + kQTiles + t); }
-  __device__ uint32_t bar_o(int t) const { return bar(1 + 2 * Cfg<D>::kSlots + 2 * kQTiles + t); }
-  __device__ uint32_t bar_drain() const { return bar(1 + 2 * Cfg<D>::kSlots + 3 * kQTiles); }
+  __device__ uint32_t bar_qfree(int t) const { return bar(1 + t); }
+  __device__ uint32_t bar_full(int s) const { return bar(1 + kQTiles + s); }
+  __device__ uint32_t bar_empty(int s) const { return bar(1 + kQTiles + Cfg<D>::kSlots + s); }
+  __device__ uint32_t bar_s(int t) const { return bar(1 + kQTiles + 2 * Cfg<D>::kSlots + t); }
+  __device__ uint32_t bar_p(int t) const { return bar(1 + 2 * kQTiles + 2 * Cfg<D>::kSlots + t); }
+  __device__ uint32_t bar_o(int t) const { return bar(1 + 3 * kQTiles + 2 * Cfg<D>::kSlots + t); }
+  __device__ uint32_t bar_drain() const { return bar(1 + 4 * kQTiles + 2 * Cfg<D>::kSlots); }
 };
 
-// TMA producer (one thread).  Item n of the K/V stream is K_{n/2} (n even) or
-// V_{n/2} (n odd) and lives in slot n % kSlots.
+// One work unit: two 128-row query tiles of one (batch, head).
+struct Unit {
+  int bh;
+  int q0;             // first query row
+  int nk_pad;         // keys allowed by padding (<= S_kv)
+  int nkv[kQTiles];   // kv tiles each query tile visits (>= 1)
+  int n;              // max over the tiles
+};
+
+// Unit u -> coordinates.  Causal: the heaviest query pairs of every head come
+// first (longest-processing-time order).  Non-causal: a head's query tiles are
+// adjacent, so the CTAs sharing its K/V run side by side and hit in L2.
+__device__ __forceinline__ Unit make_unit(const Params& p, int u) {
+  Unit w;
+  int pair;
+  if (p.causal) {
+    pair = p.n_pairs - 1 - u / p.BH;
+    w.bh = u % p.BH;
+  } else {
+    w.bh = u / p.n_pairs;
+    pair = u % p.n_pairs;
+  }
+  w.q0 = pair * kRowsPerUnit;
+  int nk = p.S_kv;
+  if (p.kv_valid != nullptr) nk = min(max(__ldg(p.kv_valid + w.bh / p.H), 0), nk);
+  w.nk_pad = nk;
+  w.n = 1;
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    const int qs = w.q0 + t * kBM;
+    int lim = nk;  // keys any row of this tile may see
+    if (qs >= p.S_q) {
+      lim = 1;  // tile past the last query row: one kv tile, never stored
+    } else if (p.causal) {
+      lim = min(lim, min(qs + kBM, p.S_q));
+    }
+    w.nkv[t] = max(1, (lim + kBN - 1) / kBN);  // a tile with no keys still runs one (fully masked) kv tile
+    w.n = max(w.n, w.nkv[t]);
+  }
+  return w;
+}
+
+// Static snake schedule: in round r, CTA c takes unit r*G + c (r even) or
+// r*G + G-1-c (r odd), which evens out the LPT-ordered causal work.
+__device__ __forceinline__ int unit_of(int r, int c, int G) { return r * G + ((r & 1) ? (G - 1 - c) : c); }
+
+// ---------------------------------------------------------------------------
+// Roles
+// ---------------------------------------------------------------------------
+
+// TMA producer (one thread).  Per unit: Q_0, Q_1, then K_0, V_0, K_1, V_1, ...;
+// K/V item `it` (counted across units) lives in slot it % kSlots.
 template <int D>
 __device__ void load_role(const Smem<D>& sm, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                          const CUtensorMap* tmV, int bh, int q0, int S_q, int nkv, const WaitCtx& w) {
+                          const CUtensorMap* tmV, const Params& p, const WaitCtx& w) {
   using C = Cfg<D>;
   tma_prefetch_desc(tmQ);
   tma_prefetch_desc(tmK);
   tma_prefetch_desc(tmV);
-  mbar_expect_tx(sm.bar_q(), kQTiles * C::kTileBytes);
-  for (int t = 0; t < kQTiles; ++t) {
-    int y = q0 + t * kBM;
-    if (y >= S_q) y = q0;  // a tile wholly past the end reloads tile 0 (never stored)
-    for (int p = 0; p < C::kPanels; ++p) tma_load_3d(sm.q(t) + p * kPanelBytes, tmQ, sm.bar_q(), p * 64, y, bh);
-  }
-  const int n_items = 2 * nkv;
-  int n = 0;
-  for (; n < n_items; ++n) {
-    const int s = n % C::kSlots;
-    const int round = n / C::kSlots;
-    if (round > 0 && !mbar_wait(sm.bar_empty(s), (round - 1) & 1, w)) break;
-    mbar_expect_tx(sm.bar_full(s), C::kTileBytes);
-    const CUtensorMap* m = (n & 1) ? tmV : tmK;
-    const int y = (n >> 1) * kBN;
-    for (int p = 0; p < C::kPanels; ++p) tma_load_3d(sm.slot(s) + p * kPanelBytes, m, sm.bar_full(s), p * 64, y, bh);
-  }
-  // Every issued copy must land before the CTA can exit (one shared deadline).
-  bool drained = mbar_wait_drain(sm.bar_q(), 0, w);
-  for (int i = (n > C::kSlots ? n - C::kSlots : 0); i < n && drained; ++i) {
-    drained = mbar_wait_drain(sm.bar_full(i % C::kSlots), (i / C::kSlots) & 1, w);
-  }
-}
-
-// MMA issuer (one thread).
-template <int D>
-__device__ void mma_role(const Smem<D>& sm, uint32_t tmem, int nkv, const WaitCtx& w) {
-  using C = Cfg<D>;
-  constexpr uint32_t idesc_s = make_idesc_bf16(kBM, kBN, false, false);
-  constexpr uint32_t idesc_pv = make_idesc_bf16(kBM, D, false, true);
-  const uint32_t tS0 = tmem, tS1 = tmem + kBN;
-  const uint32_t tO0 = tmem + C::kOCol0, tO1 = tmem + C::kOCol0 + D;
-  bool issued = false;
-  bool ok = mbar_wait(sm.bar_q(), 0, w) && mbar_wait(sm.bar_full(0), 0, w);
-  if (ok) {
-    tc_fence_after();
-    issue_qk<D>(tS0, sm.q(0), sm.slot(0), idesc_s);
-    tc_commit(sm.bar_s(0));
-    issue_qk<D>(tS1, sm.q(1), sm.slot(0), idesc_s);
-    tc_commit(sm.bar_s(1));
-    tc_commit(sm.bar_empty(0));
-    issued = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int iv = 2 * j + 1, ik = 2 * j + 2;
-      const int sv = iv % C::kSlots, sk = ik % C::kSlots;
-      const bool has_next = j + 1 < nkv;
-      if (!mbar_wait(sm.bar_full(sv), (iv / C::kSlots) & 1, w)) break;
-      if (has_next && !mbar_wait(sm.bar_full(sk), (ik / C::kSlots) & 1, w)) break;
-      // tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T (P0 is read before S0 is overwritten:
-      // MMAs issued by one thread execute in order)
-      if (!mbar_wait(sm.bar_p(0), j & 1, w)) break;
-      tc_fence_after();
-      issue_pv<D>(tO0, tS0, sm.slot(sv), idesc_pv, j > 0);
-      tc_commit(sm.bar_o(0));
-      if (has_next) {
-        issue_qk<D>(tS0, sm.q(0), sm.slot(sk), idesc_s);
-        tc_commit(sm.bar_s(0));
-      }
-      // tile 1
-      if (!mbar_wait(sm.bar_p(1), j & 1, w)) break;
-      tc_fence_after();
-      issue_pv<D>(tO1, tS1, sm.slot(sv), idesc_pv, j > 0);
-      tc_commit(sm.bar_o(1));
-      tc_commit(sm.bar_empty(sv));
-      if (has_next) {
-        issue_qk<D>(tS1, sm.q(1), sm.slot(sk), idesc_s);
-        tc_commit(sm.bar_s(1));
-        tc_commit(sm.bar_empty(sk));
+  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  const int rounds = (p.n_units + G - 1) / G;
+  int it = 0;  // K/V items issued
+  int k = 0;   // units whose Q was issued
+  bool ok = true;
+  for (int r = 0; r < rounds && ok; ++r) {
+    const int u = unit_of(r, cta, G);
+    if (u >= p.n_units) continue;
+    const Unit un = make_unit(p, u);
+    if (k > 0) {  // the previous unit's last S MMAs have read both Q tiles
+      ok = mbar_wait(sm.bar_qfree(0), (k - 1) & 1, w) && mbar_wait(sm.bar_qfree(1), (k - 1) & 1, w);
+      if (!ok) break;
+    }
+    mbar_expect_tx(sm.bar_q(), kQTiles * C::kTileBytes);
+    for (int t = 0; t < kQTiles; ++t) {
+      int y = un.q0 + t * kBM;
+      if (y >= p.S_q) y = un.q0;  // a tile wholly past the end reloads tile 0 (never stored)
+      for (int pn = 0; pn < C::kPanels; ++pn)
+        tma_load_3d(sm.q(t) + pn * kPanelBytes, tmQ, sm.bar_q(), pn * 64, y, un.bh);
+    }
+    ++k;
+    for (int j = 0; j < un.n && ok; ++j) {
+      for (int kv = 0; kv < 2; ++kv) {
+        const int s = it % C::kSlots;
+        const int round = it / C::kSlots;
+        if (round > 0 && !mbar_wait(sm.bar_empty(s), (round - 1) & 1, w)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(sm.bar_full(s), C::kTileBytes);
+        const CUtensorMap* m = kv ? tmV : tmK;
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_3d(sm.slot(s) + pn * kPanelBytes, m, sm.bar_full(s), pn * 64, j * kBN, un.bh);
+        ++it;
       }
     }
   }
-  if (issued) {  // all MMAs this thread issued are complete before TMEM is freed
-    tc_commit(sm.bar_drain());
-    mbar_wait_drain(sm.bar_drain(), 0, w);
+  // Every issued copy must land before the CTA can exit (one shared deadline).
+  bool drained = (k == 0) || mbar_wait_drain(sm.bar_q(), (k - 1) & 1, w);
+  for (int i = (it > C::kSlots ? it - C::kSlots : 0); i < it && drained; ++i)
+    drained = mbar_wait_drain(sm.bar_full(i % C::kSlots), (i / C::kSlots) & 1, w);
+}
+
+// MMA issuer: the whole warp runs the control flow (so addresses and
+// descriptors are warp-uniform); one elected lane issues the MMAs and
+// commits.  Per unit and kv step j, for each query tile t that still has
+// keys: O_t (+)= P_t V_j, then S_t = Q_t K_{j+1}^T.  P_t is read before the
+// next S_t overwrites it because MMAs issued by one thread execute in order.
+// The first P_t V of a unit overwrites O_t only after P_t of that unit is
+// ready, which the softmax warps signal after they have read the previous
+// unit's O_t out of TMEM.
+template <int D>
+__device__ void mma_role(const Smem<D>& sm, uint32_t tmem, const Params& p, const WaitCtx& w) {
+  using C = Cfg<D>;
+  constexpr uint32_t idesc_s = make_idesc_bf16(kBM, kBN, false, false);
+  constexpr uint32_t idesc_pv = make_idesc_bf16(kBM, D, false, true);
+  const uint32_t leader = elect_one();
+  const uint32_t tS[kQTiles] = {tmem, tmem + kBN};
+  const uint32_t tO[kQTiles] = {tmem + C::kOCol0, tmem + C::kOCol0 + D};
+  const uint64_t qd[kQTiles] = {sdesc_kmajor_sw128(sm.q(0)), sdesc_kmajor_sw128(sm.q(1))};
+  const uint64_t kd0 = sdesc_kmajor_sw128(sm.slot(0));
+  const uint64_t vd0 = sdesc_mnmajor_sw128(sm.slot(0), kPanelBytes);
+  constexpr uint64_t kSlotStep = C::kTileBytes >> 4;  // descriptor distance between slots
+  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  const int rounds = (p.n_units + G - 1) / G;
+  int it = 0;                // K/V items consumed
+  int k = 0;                 // units started
+  int pc[kQTiles] = {0, 0};  // P_full phases consumed
+  bool ok = true, issued = false;
+  for (int r = 0; r < rounds && ok; ++r) {
+    const int u = unit_of(r, cta, G);
+    if (u >= p.n_units) continue;
+    const Unit un = make_unit(p, u);
+    const int sk0 = it % C::kSlots;
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_q(), k & 1, w) &&
+                                     mbar_wait(sm.bar_full(sk0), (it / C::kSlots) & 1, w));
+    if (!ok) break;
+    tc_fence_after();
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t) {  // S_t = Q_t K_0^T (S_t is free: the last P_t V was issued before)
+      issue_qk<D>(leader, tS[t], qd[t], kd0 + sk0 * kSlotStep, idesc_s);
+      tc_commit_if(leader, sm.bar_s(t));
+      if (un.nkv[t] == 1) tc_commit_if(leader, sm.bar_qfree(t));
+    }
+    issued = true;
+    tc_commit_if(leader, sm.bar_empty(sk0));
+    ++it;
+    for (int j = 0; j < un.n && ok; ++j) {
+      const int iv = it, ik = it + 1;  // V_j, K_{j+1}
+      const int sv = iv % C::kSlots, skn = ik % C::kSlots;
+      const bool has_next = j + 1 < un.n;
+      ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_full(sv), (iv / C::kSlots) & 1, w) &&
+                                       (!has_next || mbar_wait(sm.bar_full(skn), (ik / C::kSlots) & 1, w)));
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        if (!ok || j >= un.nkv[t]) continue;
+        ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_p(t), pc[t] & 1, w));
+        ++pc[t];
+        if (!ok) continue;
+        tc_fence_after();
+        issue_pv<D>(leader, tO[t], tS[t], vd0 + sv * kSlotStep, idesc_pv, j > 0);
+        tc_commit_if(leader, sm.bar_o(t));
+        if (j + 1 < un.nkv[t]) {
+          issue_qk<D>(leader, tS[t], qd[t], kd0 + skn * kSlotStep, idesc_s);
+          tc_commit_if(leader, sm.bar_s(t));
+          if (j + 2 == un.nkv[t]) tc_commit_if(leader, sm.bar_qfree(t));
+        }
+      }
+      if (!ok) break;
+      tc_commit_if(leader, sm.bar_empty(sv));
+      ++it;
+      if (has_next) {
+        tc_commit_if(leader, sm.bar_empty(skn));
+        ++it;
+      }
+    }
+    ++k;
+  }
+  if (issued) {  // all MMAs the leader issued are complete before TMEM is freed
+    tc_commit_if(leader, sm.bar_drain());
+    __all_sync(0xffffffffu, mbar_wait_drain(sm.bar_drain(), 0, w));
   }
 }
 
 // Softmax + epilogue for query tile t (128 threads, one query row each).
 template <int D>
-__device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const CUtensorMap* tmO, const Params& p,
-                             int bh, int q0, int nk_pad, int nkv, const WaitCtx& w) {
+__device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Params& p, const WaitCtx& w) {
   using C = Cfg<D>;
   const int r = static_cast<int>(threadIdx.x) - kBM * (1 + t);  // row in tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_off + t * kBN;
   const uint32_t tO = tmem + lane_off + C::kOCol0 + t * D;
-  const int qs = q0 + t * kBM;
-  const int row = qs + r;
-  int lim = nk_pad;  // keys j < lim are allowed for this row
-  if (p.causal) lim = min(lim, row + 1);
   const float c = p.scale_log2;
-
-  float m_c = -INFINITY;  // running max, in scaled log2 units, as used for P
-  float l = 0.f;          // running sum of P relative to m_c
+  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  const int rounds = (p.n_units + G - 1) / G;
+  int cnt = 0;  // kv tiles this query tile has processed (S_full / O_done phases)
   bool ok = true;
-  for (int j = 0; j < nkv; ++j) {
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_s(t), j & 1, w));
-    if (!ok) break;
-    tc_fence_after();
-    uint32_t sr[kBN];
-    tmem_ld32(tS + 0, sr + 0);
-    tmem_ld32(tS + 32, sr + 32);
-    tmem_ld32(tS + 64, sr + 64);
-    tmem_ld32(tS + 96, sr + 96);
-    tmem_wait_ld();
-    float s[kBN];
-#pragma unroll
-    for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sr[i]);
+  for (int rr = 0; rr < rounds && ok; ++rr) {
+    const int u = unit_of(rr, cta, G);
+    if (u >= p.n_units) continue;
+    const Unit un = make_unit(p, u);
+    const int qs = un.q0 + t * kBM;
+    const int row = qs + r;
+    int lim = un.nk_pad;  // keys j < lim are allowed for this row
+    if (p.causal) lim = min(lim, row + 1);
+    const int nkv = t ? un.nkv[1] : un.nkv[0];
 
-    const int kbase = j * kBN;
-    if (kbase + kBN > nk_pad || (p.causal && kbase + kBN - 1 > qs)) {
-      const int lj = lim - kbase;
+    float m_c = -INFINITY;  // running max, in scaled log2 units, as used for P
+    float l = 0.f;          // running sum of P relative to m_c
+    for (int j = 0; j < nkv; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_s(t), (cnt + j) & 1, w));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[kBN];
+      tmem_ld32(tS + 0, sr + 0);
+      tmem_ld32(tS + 32, sr + 32);
+      tmem_ld32(tS + 64, sr + 64);
+      tmem_ld32(tS + 96, sr + 96);
+      tmem_wait_ld();
+      float s[kBN];
 #pragma unroll
-      for (int i = 0; i < kBN; ++i) s[i] = (i < lj) ? s[i] : -INFINITY;
-    }
-    float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-    for (int i = 4; i < kBN; i += 4) {
-      mx0 = fmaxf(mx0, s[i]);
-      mx1 = fmaxf(mx1, s[i + 1]);
-      mx2 = fmaxf(mx2, s[i + 2]);
-      mx3 = fmaxf(mx3, s[i + 3]);
-    }
-    const float new_mc = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
-    float alpha = 1.f;
-    bool rescale_o = false;
-    if (new_mc > m_c + kRescaleLog2) {  // also taken on the first tile (m_c = -inf)
-      alpha = ex2_approx(m_c - new_mc);
-      rescale_o = j > 0;  // O holds data only after the first P.V
-      m_c = new_mc;
-    }
-    const float mc = (m_c == -INFINITY) ? 0.f : m_c;
+      for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sr[i]);
 
-    uint32_t pk[kBN / 2];
-    float sum0 = 0.f, sum1 = 0.f;
+      const int kbase = j * kBN;
+      if (kbase + kBN > un.nk_pad || (p.causal && kbase + kBN - 1 > qs)) {
+        const int lj = lim - kbase;
 #pragma unroll
-    for (int i = 0; i < kBN / 2; ++i) {
-      const float a = ex2_approx(fmaf(s[2 * i], c, -mc));
-      const float b = ex2_approx(fmaf(s[2 * i + 1], c, -mc));
-      sum0 += a;
-      sum1 += b;
-      pk[i] = pack_bf16x2(a, b);
-    }
-    l = l * alpha + (sum0 + sum1);
-    tmem_st32(tS + 0, pk + 0);
-    tmem_st32(tS + 32, pk + 32);
-    tmem_wait_st();
+        for (int i = 0; i < kBN; ++i) s[i] = (i < lj) ? s[i] : -INFINITY;
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kBN; i += 8) {
+        mx0 = max3f(mx0, s[i], s[i + 1]);
+        mx1 = max3f(mx1, s[i + 2], s[i + 3]);
+        mx2 = max3f(mx2, s[i + 4], s[i + 5]);
+        mx3 = max3f(mx3, s[i + 6], s[i + 7]);
+      }
+      const float new_mc = max3f(mx0, mx1, fmaxf(mx2, mx3)) * c;
+      float alpha = 1.f;
+      bool rescale_o = false;
+      if (new_mc > m_c + kRescaleLog2) {  // also taken on the first tile (m_c = -inf)
+        alpha = ex2_approx(m_c - new_mc);
+        rescale_o = j > 0;  // O holds data only after the first P.V of the unit
+        m_c = new_mc;
+      }
+      const float mc = (m_c == -INFINITY) ? 0.f : m_c;
 
-    // Lazy correction: O is rescaled only when some row's max grew by > 2^8.
-    if (__any_sync(0xffffffffu, rescale_o)) {
-      ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (j - 1) & 1, w));
-      if (ok) {
-        tc_fence_after();
+      // p = 2^(s*c - m): one FFMA and one MUFU.EX2 per score; the fp32 p
+      // feed the row sum, their bf16 pairs feed the P.V MMA.
+      uint32_t pk[kBN / 2];
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < kBN / 2; ++i) {
+        const float a = ex2_approx(fmaf(s[2 * i], c, -mc));
+        const float b = ex2_approx(fmaf(s[2 * i + 1], c, -mc));
+        sum0 += a;
+        sum1 += b;
+        pk[i] = pack_bf16x2(a, b);
+      }
+      const float sa = sum0, sb = sum1;
+      l = l * alpha + (sa + sb);
+      tmem_st32(tS + 0, pk + 0);
+      tmem_st32(tS + 32, pk + 32);
+      tmem_wait_st();
+
+      // Lazy correction: O is rescaled only when some row's max grew by > 2^8.
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (cnt + j - 1) & 1, w));
+        if (ok) {
+          tc_fence_after();
+          const uint64_t a2 = pack_f32x2(alpha, alpha);
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + cc, o);
-          tmem_wait_ld();
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + cc, o);
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              unpack_f32x2(mul_f32x2(pack_f32x2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
+              o[i] = __float_as_uint(x0);
+              o[i + 1] = __float_as_uint(x1);
+            }
+            tmem_st32(tO + cc, o);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(sm.bar_p(t));
+      if (!ok) break;
+    }
+
+    // Epilogue: read O out of TMEM in two halves (after the second, O_t is
+    // free for the next unit), scale by 1/l, round to bf16 and store the row
+    // with 16-byte stores; LSE is (m + log2 l) ln 2, one coalesced fp32 store
+    // per row.
+    bool have_o = ok;
+    if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (cnt + nkv - 1) & 1, w));
+    cnt += nkv;
+    if (have_o) tc_fence_after();
+    float inv_l = 0.f, lse = -INFINITY;
+    if (l > 0.f) {
+      inv_l = 1.f / l;
+      lse = (m_c + log2f(l)) * kLn2;
+    }
+    const int64_t grow = static_cast<int64_t>(un.bh) * p.S_q + row;
+    uint16_t* dst = p.o + grow * D;
+    const uint64_t il2 = pack_f32x2(inv_l, inv_l);
+    constexpr int kHalf = D / 2;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t o[kHalf];
+      if (have_o) {
+#pragma unroll
+        for (int cc = 0; cc < kHalf; cc += 32) tmem_ld32(tO + h * kHalf + cc, o + cc);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) o[i] = 0u;
+      }
+      if (row < p.S_q) {
+#pragma unroll
+        for (int q = 0; q < kHalf / 8; ++q) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x0, x1;
+            unpack_f32x2(
+                mul_f32x2(pack_f32x2(__uint_as_float(o[8 * q + 2 * e]), __uint_as_float(o[8 * q + 2 * e + 1])), il2),
+                x0, x1);
+            wv[e] = pack_bf16x2(x0, x1);
+          }
+          st_global_v4(dst + h * kHalf + 8 * q, wv[0], wv[1], wv[2], wv[3]);
+        }
       }
     }
-    tc_fence_before();
-    mbar_arrive(sm.bar_p(t));
-    if (!ok) break;
+    if (row < p.S_q) p.lse[grow] = lse;
   }
-
-  // Epilogue: O / l -> bf16 -> swizzled smem (reusing this tile's Q buffer) ->
-  // TMA store; LSE = (m + log2 l) ln 2, one coalesced fp32 store per row.
-  float inv_l = 0.f, lse = -INFINITY;
-  if (l > 0.f) {
-    inv_l = 1.f / l;
-    lse = (m_c + log2f(l)) * kLn2;
-  }
-  bool have_o = ok && nkv > 0;
-  if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (nkv - 1) & 1, w));
-  if (have_o) tc_fence_after();
-  const uint32_t stage = sm.q(t);
-#pragma unroll 1
-  for (int cc = 0; cc < D; cc += 32) {
-    uint32_t o[32];
-    if (have_o) {
-      tmem_ld32(tO + cc, o);
-      tmem_wait_ld();
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = 0u;
-    }
-    uint32_t wv[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      wv[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-    const uint32_t panel = stage + static_cast<uint32_t>((cc >> 6) * kPanelBytes) + static_cast<uint32_t>(r * 128);
-    const int chunk0 = (cc & 63) >> 3;  // 16-byte chunk of column cc within the 128-byte row
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t addr = panel + static_cast<uint32_t>(((chunk0 + u) ^ (r & 7)) << 4);
-      st_shared_v4(addr, wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
-    }
-  }
-  fence_proxy_async_smem();
-  named_bar_sync(1 + t, kBM);
-  if (r == 0 && qs < p.S_q) {
-    for (int pn = 0; pn < C::kPanels; ++pn) tma_store_3d(tmO, stage + pn * kPanelBytes, pn * 64, qs, bh);
-    bulk_commit();
-    bulk_wait_read0();
-  }
-  if (row < p.S_q) p.lse[static_cast<int64_t>(bh) * p.S_q + row] = lse;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tmV, const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -613,16 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
-  const int bh = static_cast<int>(blockIdx.x) / p.n_pairs;
-  const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x) % p.n_pairs;  // heaviest first
-  const int q0 = pair * kRowsPerCta;
-  const int b = bh / p.H;
-
-  int nk_pad = p.S_kv;  // keys allowed by padding
-  if (p.kv_valid != nullptr) nk_pad = min(max(p.kv_valid[b], 0), p.S_kv);
-  int nk = nk_pad;  // keys any row of this CTA can see
-  if (p.causal) nk = min(nk, min(q0 + kRowsPerCta, p.S_q));
-  const int nkv = (nk + kBN - 1) / kBN;
 
   if (threadIdx.x == 0) {
     mbar_init(sm.bar_q(), 1);
@@ -631,6 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sm.bar_empty(s), 1);
     }
     for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(sm.bar_qfree(t), 1);
       mbar_init(sm.bar_s(t), 1);
       mbar_init(sm.bar_p(t), kBM);
       mbar_init(sm.bar_o(t), 1);
@@ -650,11 +797,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx w{p.timeout_ns, misc + 1};
 
   if (warp == 0) {
-    if (lane == 0 && nkv > 0) load_role<D>(sm, &tmQ, &tmK, &tmV, bh, q0, p.S_q, nkv, w);
+    if (lane == 0) load_role<D>(sm, &tmQ, &tmK, &tmV, p, w);
   } else if (warp == 1) {
-    if (lane == 0 && nkv > 0) mma_role<D>(sm, tmem, nkv, w);
+    mma_role<D>(sm, tmem, p, w);
   } else if (warp >= 4) {
-    softmax_role<D>(sm, (warp - 4) >> 2, tmem, &tmO, p, bh, q0, nk_pad, nkv, w);
+    softmax_role<D>(sm, (warp - 4) >> 2, tmem, p, w);
   }
 
   tc_fence_before();
@@ -723,16 +870,19 @@ bool encode_3d(CUtensorMap* m, const void* ptr, int D, int S, int64_t BH) {
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, 2 unsupported
+std::atomic<int> g_dev_sms[kMaxDevices];
 
-// Checks the device is sm_103 and sets the kernels' shared-memory limits once.
+// Checks the device is sm_103, records its SM count and sets the kernels'
+// shared-memory limits, once per device.
 attn_status_t prepare_device(int dev) {
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
   const int st = g_dev_state[dev].load(std::memory_order_acquire);
   if (st == 1) return ATTN_OK;
   if (st == 2) return ATTN_ERR_UNSUPPORTED;
-  int major = 0, minor = 0;
+  int major = 0, minor = 0, sms = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return ATTN_ERR_DEVICE;
   if (major != 10 || minor != 3) {
     g_dev_state[dev].store(2, std::memory_order_release);
@@ -743,6 +893,7 @@ attn_status_t prepare_device(int dev) {
       cudaFuncSetAttribute(attn_fwd_sm103a<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128>::kSmemBytes) != cudaSuccess)
     return ATTN_ERR_DEVICE;
+  g_dev_sms[dev].store(std::max(1, sms), std::memory_order_relaxed);
   g_dev_state[dev].store(1, std::memory_order_release);
   return ATTN_OK;
 }
@@ -751,24 +902,26 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 template <int D>
 attn_status_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S_q,
-                     int S_kv, float scale, int causal, const int32_t* kv_valid_len, cudaStream_t stream) {
+                     int S_kv, float scale, int causal, const int32_t* kv_valid_len, int sms, cudaStream_t stream) {
   const int64_t BH = static_cast<int64_t>(B) * H;
-  CUtensorMap tq, tk, tv, to;
-  if (!encode_3d(&tq, q, D, S_q, BH) || !encode_3d(&tk, k, D, S_kv, BH) || !encode_3d(&tv, v, D, S_kv, BH) ||
-      !encode_3d(&to, o, D, S_q, BH))
+  CUtensorMap tq, tk, tv;
+  if (!encode_3d(&tq, q, D, S_q, BH) || !encode_3d(&tk, k, D, S_kv, BH) || !encode_3d(&tv, v, D, S_kv, BH))
     return ATTN_ERR_LAUNCH;
   Params prm;
+  prm.o = static_cast<uint16_t*>(o);
   prm.lse = lse;
   prm.kv_valid = kv_valid_len;
   prm.S_q = S_q;
   prm.S_kv = S_kv;
   prm.H = H;
-  prm.n_pairs = (S_q + kRowsPerCta - 1) / kRowsPerCta;
+  prm.BH = static_cast<int>(BH);
+  prm.n_pairs = (S_q + kRowsPerUnit - 1) / kRowsPerUnit;
+  prm.n_units = static_cast<int>(BH * prm.n_pairs);
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   prm.causal = causal;
   prm.timeout_ns = kDefaultTimeoutNs;
-  const int64_t grid = BH * prm.n_pairs;
-  attn_fwd_sm103a<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
+  const int grid = std::min(prm.n_units, sms);  // persistent: at most one CTA per SM
+  attn_fwd_sm103a<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -805,7 +958,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     return ATTN_ERR_ALIGNMENT;
   const int64_t BH = static_cast<int64_t>(B) * H;
   if (BH > INT_MAX) return ATTN_ERR_UNSUPPORTED;
-  const int64_t n_pairs = (static_cast<int64_t>(S_q) + kRowsPerCta - 1) / kRowsPerCta;
+  const int64_t n_pairs = (static_cast<int64_t>(S_q) + kRowsPerUnit - 1) / kRowsPerUnit;
   if (BH * n_pairs > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   if (S_q == 0) return ATTN_OK;
 
@@ -822,8 +975,9 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
   }
   if (!get_encoder()) return ATTN_ERR_DEVICE;
-  if (D == 64) return launch<64>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, st);
-  return launch<128>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, st);
+  const int sms = g_dev_sms[dev].load(std::memory_order_relaxed);
+  if (D == 64) return launch<64>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, st);
+  return launch<128>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, st);
 }
 
 attn_status_t attn_fwd_debug_status(void* stream) {
