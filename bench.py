@@ -50,7 +50,8 @@ UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAK_TFLOPS = 1900.0
 
-# name -> B, H, S (S_q = S_kv), D, modes (causal flags), seed, q/k multipliers, kv_valid_len
+# name -> B, H, S (= S_q; S_kv defaults to S), D, modes (causal flags), seed, q/k multipliers,
+# kv_valid_len, splits (key chunks per query pair; "auto" = attn_fwd_splitkv_suggest)
 WORKLOADS = {
     "b4_h16_s1024_d64": dict(B=4, H=16, S=1024, D=64, modes=(False, True), seed=2),
     "b4_h16_s1024_d64_qx8": dict(B=4, H=16, S=1024, D=64, modes=(False, True), seed=3, q_mult=8.0),
@@ -59,6 +60,11 @@ WORKLOADS = {
                                      valid=(8192, 5000)),
     "b1_h32_s32768_d128_qkx2": dict(B=1, H=32, S=32768, D=128, modes=(True, False), seed=6,
                                     q_mult=2.0, k_mult=2.0),
+    # one query pair per head against 32k keys: 8 work units for 152 SMs unless the keys are split
+    "b1_h8_q256_kv32768_d128_splitkv": dict(B=1, H=8, S=256, S_kv=32768, D=128, modes=(False,), seed=7,
+                                            splits="auto"),
+    "b1_h8_q256_kv32768_d128_nosplit": dict(B=1, H=8, S=256, S_kv=32768, D=128, modes=(False,), seed=7,
+                                            splits=1),
 }
 DEFAULT_WORKLOAD = "b4_h16_s1024_d64"
 
@@ -78,14 +84,18 @@ def allowed_pairs(B, H, S_q, S_kv, causal, valid=None):
     return total
 
 
+def s_kv(w):
+    return w.get("S_kv", w["S"])
+
+
 def alg_flops(w, causal):
-    return 4 * w["D"] * allowed_pairs(w["B"], w["H"], w["S"], w["S"], causal, w.get("valid"))
+    return 4 * w["D"] * allowed_pairs(w["B"], w["H"], w["S"], s_kv(w), causal, w.get("valid"))
 
 
 def alg_bytes(w, causal):
     """Q + valid K/V + O (bf16) + LSE (fp32) of one forward pass."""
     B, H, S, D = w["B"], w["H"], w["S"], w["D"]
-    kv = sum(min(w["valid"][b], S) if w.get("valid") else S for b in range(B))
+    kv = sum(min(w["valid"][b], s_kv(w)) if w.get("valid") else s_kv(w) for b in range(B))
     return H * (2 * S * D * 2 * B + 2 * kv * D * 2 + S * 4 * B)
 
 
@@ -213,7 +223,7 @@ def oracle_sample(w, q_bits, k_bits, v_bits, target_s, modes):
     def row_flops(rows, causal):
         b = rows // (H * S)
         i = rows % S
-        n = np.full(rows.shape, S) if valid is None else np.asarray(valid)[b]
+        n = np.full(rows.shape, s_kv(w)) if valid is None else np.minimum(np.asarray(valid)[b], s_kv(w))
         keys = np.minimum(n, i + 1) if causal else n
         return 4.0 * D * float(keys.sum())
 
@@ -252,7 +262,7 @@ def run_reference(args, w, rank):
     import numpy as np
     import seeded_inputs as si
 
-    q, k, v = si.qkv_bf16(w["seed"], w["B"], w["H"], w["S"], w["S"], w["D"],
+    q, k, v = si.qkv_bf16(w["seed"], w["B"], w["H"], w["S"], s_kv(w), w["D"],
                           w.get("q_mult", 1.0), w.get("k_mult", 1.0))
     per_step = max(0.2, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -317,18 +327,29 @@ def main():
     attn.load()
 
     B, H, S, D = w["B"], w["H"], w["S"], w["D"]
+    S_kv = s_kv(w)
     modes = w["modes"]
     scale = 1.0 / math.sqrt(D)
-    q, k, v = si.qkv_bf16_torch(w["seed"], B, H, S, S, D, w.get("q_mult", 1.0), w.get("k_mult", 1.0),
+    q, k, v = si.qkv_bf16_torch(w["seed"], B, H, S, S_kv, D, w.get("q_mult", 1.0), w.get("k_mult", 1.0),
                                 device=dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
     kvl = torch.tensor(w["valid"], dtype=torch.int32, device=dev) if w.get("valid") else None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    splits = w.get("splits", 1)
+    if splits == "auto":
+        splits = attn.attn_fwd_splitkv_suggest(B, H, S, S_kv, D, any(modes))
+    ws_bytes = attn.attn_fwd_splitkv_workspace_bytes(B, H, S, D, splits) if splits > 1 else 0
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if splits > 1 else None
+    kernels_per_call = 2 if splits > 1 else 1  # key-split calls add the merge kernel
 
     def launch(causal):
-        attn.attn_fwd(q, k, v, o, lse, B, H, S, S, D, scale, causal, kvl, stream)
+        if splits > 1:
+            attn.attn_fwd_splitkv(q, k, v, o, lse, B, H, S, S_kv, D, scale, causal, kvl, splits, ws, ws_bytes,
+                                  stream)
+        else:
+            attn.attn_fwd(q, k, v, o, lse, B, H, S, S_kv, D, scale, causal, kvl, stream)
 
     # host buffers for the end-to-end leg
     hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
@@ -416,7 +437,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V drawn on the device)",
-        "config": {"workload": args.workload, "B": B, "H": H, "S_q": S, "S_kv": S, "D": D,
+        "config": {"workload": args.workload, "B": B, "H": H, "S_q": S, "S_kv": S_kv, "D": D,
+                   "kv_splits": splits,
                    "scale": scale, "modes": ["causal" if c else "non-causal" for c in modes],
                    "kv_valid_len": list(w["valid"]) if w.get("valid") else None,
                    "q_mult": w.get("q_mult", 1.0), "k_mult": w.get("k_mult", 1.0),
@@ -426,9 +448,11 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
                      "alg_bytes_per_launch": sum(alg_bytes(w, c) for c in modes) / n_l,
-                     "kernel": f"attn_fwd_sm103a<{D}>", "peak_source": peak_src},
+                     "kernel": (f"attn_fwd_sm103a<{D}>" if splits == 1 else
+                                f"attn_fwd_sm103a<{D}, split> + attn_merge_kernel<{D}> (one call, both timed)"),
+                     "peak_source": peak_src},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * n_l,
+        "gpu_launches": args.steps * n_l * kernels_per_call,
         "clocks": clocks,
     }
 

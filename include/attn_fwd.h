@@ -73,6 +73,53 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int B, int H, int S_q, int S_kv, int D, float scale, int causal,
                        const int32_t* kv_valid_len, void* stream);
 
+/*
+ * attn_fwd_splitkv -- the same result as attn_fwd, with the keys of every
+ * query tile split into `n_splits` contiguous chunks of whole 128-key tiles
+ * that are computed independently (more parallel work when B*H*ceil(S_q/256)
+ * is small next to the SM count) and then merged as attn_merge does.
+ *   Keys are walked block by block with running softmax statistics ("Flash
+ *   attention" glossary page, paragraph 2); combining per-chunk (O, LSE)
+ *   pairs by their log-sum-exp is the per-device step of the distributed
+ *   ("ring") form of the same tiling (same page, paragraph 4).
+ *
+ *   n_splits        1 .. 64; 1 calls attn_fwd (workspace unused).
+ *   workspace       caller-owned device buffer, 16-byte aligned, at least
+ *                   attn_fwd_splitkv_workspace_bytes(B, H, S_q, D, n_splits)
+ *                   bytes; holds fp32 partial O [n_splits][B*H*S_q][D] and
+ *                   partial LSE [n_splits][B*H*S_q].  Overwritten.
+ *   other arguments as attn_fwd.  Asynchronous (two kernel launches); argument
+ *   errors are reported before anything is launched.  Calls that share a
+ *   workspace must be ordered on one stream.
+ */
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int S_q, int S_kv, int D, float scale, int causal,
+                               const int32_t* kv_valid_len, int n_splits, void* workspace,
+                               uint64_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_fwd_splitkv needs (0 for invalid arguments). */
+uint64_t attn_fwd_splitkv_workspace_bytes(int B, int H, int S_q, int D, int n_splits);
+
+/*
+ * A split count that fills the current device for this shape: 1 when the
+ * unsplit work already covers every SM, else enough chunks to do so, with at
+ * least 4 kv tiles per chunk (at most 64).
+ */
+int attn_fwd_splitkv_suggest(int B, int H, int S_q, int S_kv, int D, int causal);
+
+/*
+ * attn_merge -- combine attention results computed over disjoint key sets:
+ *   lse = ln sum_k exp(lse_k),  O = sum_k exp(lse_k - lse) O_k.
+ *   o_parts    device fp32 [n_parts][rows][D], 16-byte aligned
+ *   lse_parts  device fp32 [n_parts][rows] (natural log; -inf = no keys)
+ *   o          device bf16 [rows][D], 16-byte aligned, written
+ *   lse        device fp32 [rows], written
+ * n_parts 1 .. 4096, D 64 or 128.  A row whose parts are all -inf gets O = 0
+ * and LSE = -inf.  Asynchronous.
+ */
+attn_status_t attn_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t rows,
+                         int D, void* o, float* lse, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* attn_status_str(attn_status_t status);
 

@@ -20,7 +20,8 @@ ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_DEVICE = 6
 
 # every extern "C" function include/attn_fwd.h declares
-EXPORTED = ("attn_fwd", "attn_status_str", "attn_fwd_debug_status",
+EXPORTED = ("attn_fwd", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
+            "attn_fwd_splitkv_suggest", "attn_merge", "attn_status_str", "attn_fwd_debug_status",
             "attn_watchdog_selftest", "attn_fwd_abi_version")
 
 _lock = threading.Lock()
@@ -48,6 +49,15 @@ def load() -> ctypes.CDLL:
             p, i = ctypes.c_void_p, ctypes.c_int
             lib.attn_fwd.restype = i
             lib.attn_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p, p]
+            u64, i64 = ctypes.c_uint64, ctypes.c_int64
+            lib.attn_fwd_splitkv.restype = i
+            lib.attn_fwd_splitkv.argtypes = [p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p, i, p, u64, p]
+            lib.attn_fwd_splitkv_workspace_bytes.restype = u64
+            lib.attn_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
+            lib.attn_fwd_splitkv_suggest.restype = i
+            lib.attn_fwd_splitkv_suggest.argtypes = [i, i, i, i, i, i]
+            lib.attn_merge.restype = i
+            lib.attn_merge.argtypes = [p, p, i, i64, i, p, p, p]
             lib.attn_status_str.restype = ctypes.c_char_p
             lib.attn_status_str.argtypes = [i]
             lib.attn_fwd_debug_status.restype = i
@@ -93,6 +103,44 @@ def attn_fwd(q, k, v, o, lse, B: int, H: int, S_q: int, S_kv: int, D: int, scale
                          _addr(kv_valid_len), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, B: int, H: int, S_q: int, S_kv: int, D: int, scale: float,
+                     causal: bool, kv_valid_len, n_splits: int, workspace, workspace_bytes: int,
+                     stream=None) -> None:
+    """Enqueue the key-split forward pass (see include/attn_fwd.h)."""
+    st = load().attn_fwd_splitkv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
+                                 int(S_q), int(S_kv), int(D), float(scale), int(bool(causal)),
+                                 _addr(kv_valid_len), int(n_splits), _addr(workspace),
+                                 int(workspace_bytes), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_splitkv")
+
+
+def attn_fwd_splitkv_workspace_bytes(B: int, H: int, S_q: int, D: int, n_splits: int) -> int:
+    return int(load().attn_fwd_splitkv_workspace_bytes(int(B), int(H), int(S_q), int(D), int(n_splits)))
+
+
+def attn_fwd_splitkv_suggest(B: int, H: int, S_q: int, S_kv: int, D: int, causal: bool) -> int:
+    return int(load().attn_fwd_splitkv_suggest(int(B), int(H), int(S_q), int(S_kv), int(D),
+                                               int(bool(causal))))
+
+
+def attn_merge(o_parts, lse_parts, n_parts: int, rows: int, D: int, o, lse, stream=None) -> None:
+    """Enqueue the log-sum-exp merge of per-key-set results (see include/attn_fwd.h)."""
+    st = load().attn_merge(_addr(o_parts), _addr(lse_parts), int(n_parts), int(rows), int(D),
+                           _addr(o), _addr(lse), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_merge")
+
+
+def call_status(fn, *args, **kwargs) -> int:
+    """Run one of the raising wrappers above and return its status instead."""
+    try:
+        fn(*args, **kwargs)
+    except AttnError as e:
+        return e.status
+    return ATTN_OK
 
 
 def attn_fwd_status(*args, **kwargs) -> int:

@@ -11,11 +11,12 @@ from . import _lib
 
 
 def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
-                      kv_valid_len=None, out=None, lse=None, stream=None):
+                      kv_valid_len=None, out=None, lse=None, stream=None, n_splits: int | None = None):
     """O and LSE for bf16 CUDA tensors q [B,H,S_q,D], k/v [B,H,S_kv,D].
 
-    kv_valid_len: int32 CUDA tensor [B] or None.  Returns (o, lse) with o bf16
-    [B,H,S_q,D] and lse fp32 [B,H,S_q].
+    kv_valid_len: int32 CUDA tensor [B] or None.  n_splits: key chunks (None
+    picks attn_fwd_splitkv_suggest's count; more than 1 takes a torch-allocated
+    workspace).  Returns (o, lse) with o bf16 [B,H,S_q,D] and lse fp32 [B,H,S_q].
     """
     import torch
 
@@ -40,5 +41,13 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
         lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    _lib.attn_fwd(q, k, v, out, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len, stream)
+    if n_splits is None:
+        n_splits = _lib.attn_fwd_splitkv_suggest(B, H, S_q, S_kv, D, causal)
+    if n_splits > 1:
+        nbytes = _lib.attn_fwd_splitkv_workspace_bytes(B, H, S_q, D, n_splits)
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+        _lib.attn_fwd_splitkv(q, k, v, out, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len,
+                              n_splits, ws, nbytes, stream)
+    else:
+        _lib.attn_fwd(q, k, v, out, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len, stream)
     return out, lse

@@ -96,10 +96,13 @@ struct Params {
   int H;
   int BH;
   int n_pairs;           // query-tile pairs per (b, h)
-  int n_units;           // BH * n_pairs
+  int n_splits;          // key chunks per query pair (1 = no split)
+  int n_units;           // BH * n_pairs * n_splits
   float scale_log2;      // scale * log2(e)
   int causal;
   unsigned long long timeout_ns;
+  float* o_part;         // split mode: fp32 [n_splits][BH * S_q][D]
+  float* lse_part;       // split mode: fp32 [n_splits][BH * S_q]
 };
 
 }  // namespace
@@ -420,15 +423,26 @@ struct Unit {
   int bh;
   int q0;             // first query row
   int nk_pad;         // keys allowed by padding (<= S_kv)
-  int nkv[kQTiles];   // kv tiles each query tile visits (>= 1)
+  int split;          // key chunk (0 without splitting)
+  int j0;             // first kv tile of the chunk
+  int mask_all;       // the chunk lies past every key this unit may see
+  int nkv[kQTiles];   // kv tiles each query tile visits from j0 (>= 1)
   int n;              // max over the tiles
 };
 
 // Unit u -> coordinates.  Causal: the heaviest query pairs of every head come
 // first (longest-processing-time order).  Non-causal: a head's query tiles are
-// adjacent, so the CTAs sharing its K/V run side by side and hit in L2.
+// adjacent, so the CTAs sharing its K/V run side by side and hit in L2.  With
+// key splitting, the chunks of one query pair are adjacent units; chunk s of
+// a pair whose tiles see at most n kv tiles covers kv tiles
+// [s*ceil(n/S), min((s+1)*ceil(n/S), n)).
 __device__ __forceinline__ Unit make_unit(const Params& p, int u) {
   Unit w;
+  w.split = 0;
+  if (p.n_splits > 1) {
+    w.split = u % p.n_splits;
+    u /= p.n_splits;
+  }
   int pair;
   if (p.causal) {
     pair = p.n_pairs - 1 - u / p.BH;
@@ -441,7 +455,8 @@ __device__ __forceinline__ Unit make_unit(const Params& p, int u) {
   int nk = p.S_kv;
   if (p.kv_valid != nullptr) nk = min(max(__ldg(p.kv_valid + w.bh / p.H), 0), nk);
   w.nk_pad = nk;
-  w.n = 1;
+  int tiles[kQTiles];  // kv tiles holding keys each query tile may see
+  int n_all = 1;
 #pragma unroll
   for (int t = 0; t < kQTiles; ++t) {
     const int qs = w.q0 + t * kBM;
@@ -451,7 +466,26 @@ __device__ __forceinline__ Unit make_unit(const Params& p, int u) {
     } else if (p.causal) {
       lim = min(lim, min(qs + kBM, p.S_q));
     }
-    w.nkv[t] = max(1, (lim + kBN - 1) / kBN);  // a tile with no keys still runs one (fully masked) kv tile
+    tiles[t] = (lim + kBN - 1) / kBN;
+    n_all = max(n_all, tiles[t]);
+  }
+  int lo = 0, hi = n_all;
+  if (p.n_splits > 1) {
+    const int chunk = (n_all + p.n_splits - 1) / p.n_splits;
+    lo = w.split * chunk;
+    hi = min(lo + chunk, n_all);
+  }
+  w.mask_all = lo >= hi;  // an empty chunk: one kv tile, every key masked
+  if (w.mask_all) {
+    lo = 0;
+    hi = 1;
+  }
+  w.j0 = lo;
+  w.n = 1;
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    // a tile with no keys in the chunk still runs one (fully masked) kv tile
+    w.nkv[t] = max(1, min(hi, tiles[t]) - lo);
     w.n = max(w.n, w.nkv[t]);
   }
   return w;
@@ -506,7 +540,7 @@ __device__ void load_role(const Smem<D>& sm, const CUtensorMap* tmQ, const CUten
         mbar_expect_tx(sm.bar_full(s), C::kTileBytes);
         const CUtensorMap* m = kv ? tmV : tmK;
         for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_3d(sm.slot(s) + pn * kPanelBytes, m, sm.bar_full(s), pn * 64, j * kBN, un.bh);
+          tma_load_3d(sm.slot(s) + pn * kPanelBytes, m, sm.bar_full(s), pn * 64, (un.j0 + j) * kBN, un.bh);
         ++it;
       }
     }
@@ -599,7 +633,8 @@ __device__ void mma_role(const Smem<D>& sm, uint32_t tmem, const Params& p, cons
 }
 
 // Softmax + epilogue for query tile t (128 threads, one query row each).
-template <int D>
+// kSplit: the unit covers one key chunk and writes fp32 O and LSE partials.
+template <int D, bool kSplit>
 __device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Params& p, const WaitCtx& w) {
   using C = Cfg<D>;
   const int r = static_cast<int>(threadIdx.x) - kBM * (1 + t);  // row in tile == TMEM lane
@@ -617,7 +652,7 @@ __device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Para
     const Unit un = make_unit(p, u);
     const int qs = un.q0 + t * kBM;
     const int row = qs + r;
-    int lim = un.nk_pad;  // keys j < lim are allowed for this row
+    int lim = un.mask_all ? 0 : un.nk_pad;  // keys j < lim are allowed for this row
     if (p.causal) lim = min(lim, row + 1);
     const int nkv = t ? un.nkv[1] : un.nkv[0];
 
@@ -637,8 +672,8 @@ __device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Para
 #pragma unroll
       for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sr[i]);
 
-      const int kbase = j * kBN;
-      if (kbase + kBN > un.nk_pad || (p.causal && kbase + kBN - 1 > qs)) {
+      const int kbase = (un.j0 + j) * kBN;
+      if (un.mask_all || kbase + kBN > un.nk_pad || (p.causal && kbase + kBN - 1 > qs)) {
         const int lj = lim - kbase;
 #pragma unroll
         for (int i = 0; i < kBN; ++i) s[i] = (i < lj) ? s[i] : -INFINITY;
@@ -721,6 +756,7 @@ __device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Para
       lse = (m_c + log2f(l)) * kLn2;
     }
     const int64_t grow = static_cast<int64_t>(un.bh) * p.S_q + row;
+    const int64_t prow = static_cast<int64_t>(un.split) * p.BH * p.S_q + grow;  // split mode
     uint16_t* dst = p.o + grow * D;
     const uint64_t il2 = pack_f32x2(inv_l, inv_l);
     constexpr int kHalf = D / 2;
@@ -735,7 +771,21 @@ __device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Para
 #pragma unroll
         for (int i = 0; i < kHalf; ++i) o[i] = 0u;
       }
-      if (row < p.S_q) {
+      if (kSplit) {  // fp32 partial O of this key chunk (already divided by its own l)
+        if (row < p.S_q) {
+          float* pdst = p.o_part + prow * D + h * kHalf;
+#pragma unroll
+          for (int q = 0; q < kHalf / 4; ++q) {
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; e += 2)
+              unpack_f32x2(mul_f32x2(pack_f32x2(__uint_as_float(o[4 * q + e]), __uint_as_float(o[4 * q + e + 1])), il2),
+                           x[e], x[e + 1]);
+            st_global_v4(pdst + 4 * q, __float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                         __float_as_uint(x[3]));
+          }
+        }
+      } else if (row < p.S_q) {
 #pragma unroll
         for (int q = 0; q < kHalf / 8; ++q) {
           uint32_t wv[4];
@@ -751,11 +801,16 @@ __device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Para
         }
       }
     }
-    if (row < p.S_q) p.lse[grow] = lse;
+    if (row < p.S_q) {
+      if (kSplit)
+        p.lse_part[prow] = lse;
+      else
+        p.lse[grow] = lse;
+    }
   }
 }
 
-template <int D>
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -801,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     mma_role<D>(sm, tmem, p, w);
   } else if (warp >= 4) {
-    softmax_role<D>(sm, (warp - 4) >> 2, tmem, p, w);
+    softmax_role<D, kSplit>(sm, (warp - 4) >> 2, tmem, p, w);
   }
 
   tc_fence_before();
@@ -819,6 +874,64 @@ __global__ void attn_fill_empty(uint16_t* o, float* lse, int64_t rows, int D) {
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     for (int d = 0; d < D; ++d) o[i * D + d] = 0;
     lse[i] = -INFINITY;
+  }
+}
+
+// Merge of attention results over disjoint key sets -- the reduction after
+// key splitting, and the per-device combine step of ring attention
+// ("Flash attention" glossary page, paragraph 4):
+//   lse = ln sum_k exp(lse_k),   O = sum_k exp(lse_k - lse) O_k.
+// One warp per row; each lane owns D/32 consecutive columns.  A part with
+// lse_k = -inf (no keys) has weight 0; a row where every part has -inf gets
+// O = 0 and LSE = -inf.  HBM-bound: n_parts * (D + 1) * 4 bytes read and
+// D * 2 + 4 bytes written per row.
+template <int D>
+__global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict__ o_parts,
+                                                         const float* __restrict__ lse_parts, int n_parts,
+                                                         int64_t rows, int64_t part_stride_rows,
+                                                         uint16_t* __restrict__ o, float* __restrict__ lse) {
+  constexpr int kPer = D / 32;
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t step = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = first; row < rows; row += step) {
+    float mx = -INFINITY;
+    for (int k = lane; k < n_parts; k += 32) mx = fmaxf(mx, __ldg(lse_parts + k * part_stride_rows + row));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    if (mx > -INFINITY) {
+      for (int k = 0; k < n_parts; ++k) {
+        const int64_t pr = k * part_stride_rows + row;
+        const float wk = expf(__ldg(lse_parts + pr) - mx);
+        wsum += wk;
+        const float* src = o_parts + pr * D + lane * kPer;
+        if (kPer == 4) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(src));
+          acc[0] += wk * v.x;
+          acc[1] += wk * v.y;
+          acc[2 % kPer] += wk * v.z;
+          acc[3 % kPer] += wk * v.w;
+        } else {
+          const float2 v = __ldg(reinterpret_cast<const float2*>(src));
+          acc[0] += wk * v.x;
+          acc[1] += wk * v.y;
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint32_t packed[kPer / 2];
+#pragma unroll
+    for (int e = 0; e < kPer / 2; ++e) packed[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+    uint16_t* dst = o + row * D + lane * kPer;
+    if (kPer == 4)
+      *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[(kPer / 2) - 1]);
+    else
+      *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    if (lane == 0) lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
   }
 }
 
@@ -888,9 +1001,13 @@ attn_status_t prepare_device(int dev) {
     g_dev_state[dev].store(2, std::memory_order_release);
     return ATTN_ERR_UNSUPPORTED;
   }
-  if (cudaFuncSetAttribute(attn_fwd_sm103a<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(attn_fwd_sm103a<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<64>::kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_sm103a<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(attn_fwd_sm103a<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<64>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128>::kSmemBytes) != cudaSuccess)
     return ATTN_ERR_DEVICE;
   g_dev_sms[dev].store(std::max(1, sms), std::memory_order_relaxed);
@@ -900,9 +1017,12 @@ attn_status_t prepare_device(int dev) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Launches the attention kernel; with n_splits > 1 it writes fp32 partials to
+// o_part / lse_part instead of o / lse.
 template <int D>
 attn_status_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S_q,
-                     int S_kv, float scale, int causal, const int32_t* kv_valid_len, int sms, cudaStream_t stream) {
+                     int S_kv, float scale, int causal, const int32_t* kv_valid_len, int sms, int n_splits,
+                     float* o_part, float* lse_part, cudaStream_t stream) {
   const int64_t BH = static_cast<int64_t>(B) * H;
   CUtensorMap tq, tk, tv;
   if (!encode_3d(&tq, q, D, S_q, BH) || !encode_3d(&tk, k, D, S_kv, BH) || !encode_3d(&tv, v, D, S_kv, BH))
@@ -916,13 +1036,57 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   prm.H = H;
   prm.BH = static_cast<int>(BH);
   prm.n_pairs = (S_q + kRowsPerUnit - 1) / kRowsPerUnit;
-  prm.n_units = static_cast<int>(BH * prm.n_pairs);
+  prm.n_splits = n_splits;
+  prm.n_units = static_cast<int>(BH * prm.n_pairs * n_splits);
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   prm.causal = causal;
   prm.timeout_ns = kDefaultTimeoutNs;
+  prm.o_part = o_part;
+  prm.lse_part = lse_part;
   const int grid = std::min(prm.n_units, sms);  // persistent: at most one CTA per SM
-  attn_fwd_sm103a<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  if (n_splits > 1)
+    attn_fwd_sm103a<D, true><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  else
+    attn_fwd_sm103a<D, false><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t rows, int D, void* o,
+                           float* lse, int sms, cudaStream_t stream) {
+  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 16);
+  if (D == 64)
+    attn_merge_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_parts, lse_parts, n_parts, rows, rows,
+                                                                            static_cast<uint16_t*>(o), lse);
+  else
+    attn_merge_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_parts, lse_parts, n_parts, rows, rows,
+                                                                             static_cast<uint16_t*>(o), lse);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// Argument checks shared by attn_fwd and attn_fwd_splitkv (nothing is launched).
+attn_status_t check_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H,
+                         int S_q, int S_kv, int D, float scale, int causal, const int32_t* kv_valid_len) {
+  if (B < 1 || H < 1 || S_q < 0 || S_kv < 0) return ATTN_ERR_INVALID_ARG;
+  // a buffer may be null only when its extent is zero (empty tensors)
+  if (S_q > 0 && (q == nullptr || o == nullptr || lse == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (S_q > 0 && S_kv > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(kv_valid_len, 4))
+    return ATTN_ERR_ALIGNMENT;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const int64_t n_pairs = (static_cast<int64_t>(S_q) + kRowsPerUnit - 1) / kRowsPerUnit;
+  if (BH * n_pairs > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+constexpr int kMaxSplits = 64;
+
+uint64_t splitkv_workspace_bytes(int64_t rows, int D, int n_splits) {
+  return static_cast<uint64_t>(n_splits) * static_cast<uint64_t>(rows) * static_cast<uint64_t>(D + 1) * 4u;
 }
 
 }  // namespace
@@ -946,20 +1110,8 @@ const char* attn_status_str(attn_status_t s) {
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S_q,
                        int S_kv, int D, float scale, int causal, const int32_t* kv_valid_len, void* stream) {
-  if (B < 1 || H < 1 || S_q < 0 || S_kv < 0) return ATTN_ERR_INVALID_ARG;
-  // a buffer may be null only when its extent is zero (empty tensors)
-  if (S_q > 0 && (q == nullptr || o == nullptr || lse == nullptr)) return ATTN_ERR_INVALID_ARG;
-  if (S_q > 0 && S_kv > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
-      !aligned(kv_valid_len, 4))
-    return ATTN_ERR_ALIGNMENT;
-  const int64_t BH = static_cast<int64_t>(B) * H;
-  if (BH > INT_MAX) return ATTN_ERR_UNSUPPORTED;
-  const int64_t n_pairs = (static_cast<int64_t>(S_q) + kRowsPerUnit - 1) / kRowsPerUnit;
-  if (BH * n_pairs > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const attn_status_t as = check_args(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len);
+  if (as != ATTN_OK) return as;
   if (S_q == 0) return ATTN_OK;
 
   int dev = 0;
@@ -967,6 +1119,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   const attn_status_t ps = prepare_device(dev);
   if (ps != ATTN_OK) return ps;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t BH = static_cast<int64_t>(B) * H;
 
   if (S_kv == 0) {
     const int64_t rows = BH * S_q;
@@ -976,8 +1129,81 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   }
   if (!get_encoder()) return ATTN_ERR_DEVICE;
   const int sms = g_dev_sms[dev].load(std::memory_order_relaxed);
-  if (D == 64) return launch<64>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, st);
-  return launch<128>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, st);
+  if (D == 64)
+    return launch<64>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, 1, nullptr, nullptr, st);
+  return launch<128>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, 1, nullptr, nullptr, st);
+}
+
+uint64_t attn_fwd_splitkv_workspace_bytes(int B, int H, int S_q, int D, int n_splits) {
+  if (B < 1 || H < 1 || S_q < 0 || (D != 64 && D != 128) || n_splits < 1 || n_splits > kMaxSplits) return 0;
+  return splitkv_workspace_bytes(static_cast<int64_t>(B) * H * S_q, D, n_splits);
+}
+
+int attn_fwd_splitkv_suggest(int B, int H, int S_q, int S_kv, int D, int causal) {
+  (void)D;
+  (void)causal;
+  if (B < 1 || H < 1 || S_q < 1 || S_kv < 1) return 1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  const int64_t units = static_cast<int64_t>(B) * H * ((S_q + kRowsPerUnit - 1) / kRowsPerUnit);
+  if (units >= sms) return 1;
+  const int64_t kv_tiles = (S_kv + kBN - 1) / kBN;
+  // fill the SMs, but keep at least 4 kv tiles per chunk so a unit's start-up stays small
+  const int64_t by_sms = (sms + units - 1) / units;
+  const int64_t by_len = std::max<int64_t>(1, kv_tiles / 4);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({by_sms, by_len, kMaxSplits})));
+}
+
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                               int S_q, int S_kv, int D, float scale, int causal, const int32_t* kv_valid_len,
+                               int n_splits, void* workspace, uint64_t workspace_bytes, void* stream) {
+  const attn_status_t as = check_args(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len);
+  if (as != ATTN_OK) return as;
+  if (n_splits < 1 || n_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t rows = BH * S_q;
+  if (n_splits > 1) {
+    if (workspace == nullptr && rows > 0) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return ATTN_ERR_ALIGNMENT;
+    if (workspace_bytes < splitkv_workspace_bytes(rows, D, n_splits)) return ATTN_ERR_INVALID_ARG;
+    if (BH * ((S_q + kRowsPerUnit - 1) / kRowsPerUnit) * n_splits > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  }
+  if (n_splits == 1 || S_q == 0 || S_kv == 0)
+    return attn_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len, stream);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+  const attn_status_t ps = prepare_device(dev);
+  if (ps != ATTN_OK) return ps;
+  if (!get_encoder()) return ATTN_ERR_DEVICE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int sms = g_dev_sms[dev].load(std::memory_order_relaxed);
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = o_part + static_cast<int64_t>(n_splits) * rows * D;
+  const attn_status_t ls =
+      D == 64 ? launch<64>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, n_splits, o_part,
+                           lse_part, st)
+              : launch<128>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, n_splits, o_part,
+                            lse_part, st);
+  if (ls != ATTN_OK) return ls;
+  return launch_merge(o_part, lse_part, n_splits, rows, D, o, lse, sms, st);
+}
+
+attn_status_t attn_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t rows, int D, void* o,
+                         float* lse, void* stream) {
+  if (n_parts < 1 || n_parts > 4096 || rows < 0) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (rows == 0) return ATTN_OK;
+  if (o_parts == nullptr || lse_parts == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(o_parts, 16) || !aligned(lse_parts, 4) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_ALIGNMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+  const attn_status_t ps = prepare_device(dev);
+  if (ps != ATTN_OK) return ps;
+  return launch_merge(o_parts, lse_parts, n_parts, rows, D, o, lse, g_dev_sms[dev].load(std::memory_order_relaxed),
+                      static_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_fwd_debug_status(void* stream) {

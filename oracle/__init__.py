@@ -3,10 +3,11 @@
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product path never does.
 
-The arithmetic lives in ``attn_ref.cpp`` (plain float64 C++, one materialised
-score row per query, two-pass softmax).  This module compiles it with the host
-C++ compiler on first use (or from ``build()``) and calls it through ctypes.
-The functions here only marshal arguments.
+The attention arithmetic lives in ``attn_ref.cpp`` (plain float64 C++, one
+materialised score row per query, two-pass softmax).  This module compiles it
+with the host C++ compiler on first use (or from ``build()``) and calls it
+through ctypes; ``merge_f64`` (the log-sum-exp merge of results over disjoint
+key sets) is plain float64 numpy here.
 
 Parity pins: ``tests/test_oracle_pins.py`` and ``tests/test_oracle_mutants.py``.
 """
@@ -118,3 +119,29 @@ def score_buffer_bytes(B: int, H: int, s: int, e: int, lib=None) -> int:
 def hardware_threads(lib=None) -> int:
     lib = lib or load_library()
     return int(lib.attn_ref_hardware_threads())
+
+
+def merge_f64(o_parts, lse_parts):
+    """Combine attention results over disjoint key sets, in float64.
+
+    o_parts: [n_parts, rows, D]; lse_parts: [n_parts, rows] (natural log,
+    -inf for a part with no keys).  Returns (o [rows, D], lse [rows]):
+    lse = ln sum_k exp(lse_k) and o = sum_k exp(lse_k - lse) o_k; a row with no
+    keys in any part gets o = 0 and lse = -inf.  This is the softmax over the
+    union of the key sets written per part ("Flash attention" glossary page,
+    paragraphs 2 and 4: running softmax statistics, and the same tiling spread
+    over devices).
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    rows = lse_parts.shape[1]
+    o = np.zeros(o_parts.shape[1:], dtype=np.float64)
+    lse = np.full(rows, -np.inf)
+    for r in range(rows):
+        m = lse_parts[:, r].max()
+        if m == -np.inf:
+            continue
+        w = np.exp(lse_parts[:, r] - m)          # weight of each part, up to a common factor
+        lse[r] = m + np.log(w.sum())
+        o[r] = (w[:, None] * o_parts[:, r, :]).sum(axis=0) / w.sum()
+    return o, lse

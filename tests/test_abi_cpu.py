@@ -101,3 +101,48 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "LIB_PATH", tmp_path / "absent.so")
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load()
+
+
+def split_call(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=2, S_q=128, S_kv=4096, D=128,
+                scale=0.1, causal=False, kv_valid_len=None, n_splits=4, workspace=FAKE,
+                workspace_bytes=attn.attn_fwd_splitkv_workspace_bytes(1, 2, 128, 128, 4))
+    args.update(kw)
+    return attn.call_status(attn.attn_fwd_splitkv, **args)
+
+
+def test_splitkv_workspace_size():
+    # fp32 partial O and LSE per split: n_splits * rows * (D + 1) * 4 bytes
+    assert attn.attn_fwd_splitkv_workspace_bytes(2, 3, 100, 64, 5) == 5 * 600 * 65 * 4
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 96, 2) == 0      # bad D
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 64, 65) == 0     # too many splits
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(n_splits=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(n_splits=65), attn.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=FAKE + 8), attn.ATTN_ERR_ALIGNMENT),
+    (dict(workspace_bytes=1000), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=80), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(S_q=0), attn.ATTN_OK),
+])
+def test_splitkv_argument_checks(kw, expect):
+    assert split_call(**kw) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(n_parts=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(rows=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(o_parts=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o_parts=FAKE + 4), attn.ATTN_ERR_ALIGNMENT),
+    (dict(o=FAKE + 2), attn.ATTN_ERR_ALIGNMENT),
+    (dict(rows=0), attn.ATTN_OK),
+])
+def test_merge_argument_checks(kw, expect):
+    args = dict(o_parts=FAKE, lse_parts=FAKE, n_parts=3, rows=100, D=64, o=FAKE, lse=FAKE)
+    args.update(kw)
+    assert attn.call_status(attn.attn_merge, **args) == expect

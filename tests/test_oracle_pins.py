@@ -246,3 +246,36 @@ def test_matches_torch_sdpa_float64(B, H, S_q, S_kv, D, causal, valid):
     logits = torch.einsum("bhid,bhjd->bhij", tq, tk) * scale
     ref_lse = torch.logsumexp(logits.masked_fill(~mask, -math.inf), dim=-1)
     np.testing.assert_allclose(lse.reshape(B, H, S_q), ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# --- merge of results over disjoint key sets ----------------------------------
+
+@pytest.mark.parametrize("cuts", [[0, 5, 17], [0, 1, 2, 17], [0, 16, 17]])
+def test_merge_of_key_chunks_equals_full_attention(cuts):
+    # Attention over keys [a, b) for consecutive chunks, merged, equals attention
+    # over all keys (non-causal, so a chunk is a plain slice of K and V).
+    B, H, S_q, S_kv, D = 2, 2, 9, 17, 8
+    q, k, v = (bits(50, (B, H, n, D), t) for n, t in ((S_q, si.TID_Q), (S_kv, si.TID_K), (S_kv, si.TID_V)))
+    o_full, l_full = oracle.attention_f64(q, k, v, 0.35, False)
+    parts = [oracle.attention_f64(q, k[:, :, a:b].copy(), v[:, :, a:b].copy(), 0.35, False)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    o, l = oracle.merge_f64([p[0] for p in parts], [p[1] for p in parts])
+    np.testing.assert_allclose(o, o_full, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l, l_full, rtol=1e-13, atol=1e-13)
+
+
+def test_merge_closed_forms():
+    o1 = np.array([[1.0, 2.0], [3.0, 4.0]])
+    o2 = np.array([[5.0, 6.0], [7.0, 8.0]])
+    # equal weights -> the average; LSE gains ln 2
+    o, l = oracle.merge_f64([o1, o2], [[0.5, -1.0], [0.5, -1.0]])
+    np.testing.assert_allclose(o, (o1 + o2) / 2)
+    np.testing.assert_allclose(l, [0.5 + math.log(2), -1.0 + math.log(2)])
+    # a part without keys (-inf) has no weight; all parts empty -> 0 / -inf
+    o, l = oracle.merge_f64([o1, o2], [[-np.inf, -np.inf], [2.0, -np.inf]])
+    np.testing.assert_array_equal(o[0], o2[0])
+    assert l[0] == 2.0 and np.isneginf(l[1]) and np.all(o[1] == 0)
+    # one part is the identity
+    o, l = oracle.merge_f64([o1], [[0.25, 7.0]])
+    np.testing.assert_array_equal(o, o1)
+    np.testing.assert_array_equal(l, [0.25, 7.0])
