@@ -69,9 +69,11 @@ def test_splitkv_agrees_with_unsplit_kernel(dev):
     q, k, v = si.qkv_bf16(920, 2, 4, 512, 4096, 128, q_mult=2.0)
     o1, l1 = run_split(q, k, v, 0.09, True, 7)
     o2, l2 = parity.gather_rows(*parity.run_cuda(q, k, v, 0.09, True))
-    # the two paths round at different points: at most two bf16 steps apart
-    assert np.all(np.abs(o1 - o2) <= 2.0 ** -7 * np.maximum(np.abs(o2), 2.0 ** -6))
+    # the two paths round P to bf16 against different running maxima, so they
+    # agree to the parity bar rather than bit for bit; LSE agrees more tightly
+    parity.compare(o1, l1, o2, l2)
     assert np.abs(l1 - l2).max() <= 1e-4
+    assert np.linalg.norm(o1 - o2) <= 3e-3 * np.linalg.norm(o2)
 
 
 def test_decode_shape_sampled_rows(dev):
