@@ -120,6 +120,39 @@ int attn_fwd_splitkv_suggest(int B, int H, int S_q, int S_kv, int D, int causal)
 attn_status_t attn_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t rows,
                          int D, void* o, float* lse, void* stream);
 
+/*
+ * attn_fwd_splitkv_static -- attn_fwd_splitkv without a caller workspace,
+ * for callers that cannot allocate device memory: code that runs where every
+ * device byte is handed out by some other component's pool and side
+ * allocations are not allowed, or where the device-wide synchronisation that
+ * cudaMalloc / cudaFree imply cannot be paid at that point.  The pages
+ * describe no counterpart; this is a deployment convenience.
+ *
+ * The partial results live in one fixed array of ATTN_STATIC_SCRATCH_BYTES
+ * (32 MiB) that is part of this library's device image; every GPU that loads
+ * the library holds it until the process exits.  This call allocates and
+ * frees nothing.  It needs n_splits * B*H*S_q * (D + 1) * 4 bytes of that
+ * array and returns ATTN_ERR_UNSUPPORTED, launching nothing, when that is
+ * more than ATTN_STATIC_SCRATCH_BYTES (use fewer splits, or attn_fwd_splitkv
+ * with your own workspace).
+ *
+ * The first call on each device looks up the array's device address with
+ * that device current (cudaGetSymbolAddress) and keeps it; make that first
+ * call before any stream capture begins.
+ *
+ * The array is shared by every call in the process and keeps whatever the
+ * last call left in it; nothing needs to start at zero, because each call
+ * writes every partial it later reads.  Calls that can run at the same time on
+ * the GPU (different streams, or different host threads without ordering)
+ * race on the array: order them on one stream.  Other arguments and the
+ * result are as attn_fwd_splitkv.
+ */
+#define ATTN_STATIC_SCRATCH_BYTES (32ull << 20)
+attn_status_t attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o,
+                                      float* lse, int B, int H, int S_q, int S_kv, int D,
+                                      float scale, int causal, const int32_t* kv_valid_len,
+                                      int n_splits, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* attn_status_str(attn_status_t status);
 

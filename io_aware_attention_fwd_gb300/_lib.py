@@ -21,7 +21,7 @@ ATTN_ERR_DEVICE = 6
 
 # every extern "C" function include/attn_fwd.h declares
 EXPORTED = ("attn_fwd", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
-            "attn_fwd_splitkv_suggest", "attn_merge", "attn_status_str", "attn_fwd_debug_status",
+            "attn_fwd_splitkv_suggest", "attn_merge", "attn_fwd_splitkv_static", "attn_status_str", "attn_fwd_debug_status",
             "attn_watchdog_selftest", "attn_fwd_abi_version")
 
 _lock = threading.Lock()
@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
             lib.attn_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
             lib.attn_fwd_splitkv_suggest.restype = i
             lib.attn_fwd_splitkv_suggest.argtypes = [i, i, i, i, i, i]
+            lib.attn_fwd_splitkv_static.restype = i
+            lib.attn_fwd_splitkv_static.argtypes = [p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_merge.restype = i
             lib.attn_merge.argtypes = [p, p, i, i64, i, p, p, p]
             lib.attn_status_str.restype = ctypes.c_char_p
@@ -132,6 +134,24 @@ def attn_merge(o_parts, lse_parts, n_parts: int, rows: int, D: int, o, lse, stre
                            _addr(o), _addr(lse), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_merge")
+
+
+# Size of the library's fixed scratch (ATTN_STATIC_SCRATCH_BYTES in the header).
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def attn_fwd_splitkv_static(q, k, v, o, lse, B: int, H: int, S_q: int, S_kv: int, D: int,
+                            scale: float, causal: bool, kv_valid_len, n_splits: int,
+                            stream=None) -> None:
+    """Key-split forward using the library's fixed scratch instead of a
+    workspace, for callers that cannot allocate device memory (see
+    include/attn_fwd.h: 32 MiB cap, one call at a time on the GPU)."""
+    st = load().attn_fwd_splitkv_static(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B),
+                                        int(H), int(S_q), int(S_kv), int(D), float(scale),
+                                        int(bool(causal)), _addr(kv_valid_len), int(n_splits),
+                                        _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_splitkv_static")
 
 
 def call_status(fn, *args, **kwargs) -> int:

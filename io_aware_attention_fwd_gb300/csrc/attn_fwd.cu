@@ -1089,6 +1089,29 @@ uint64_t splitkv_workspace_bytes(int64_t rows, int D, int n_splits) {
   return static_cast<uint64_t>(n_splits) * static_cast<uint64_t>(rows) * static_cast<uint64_t>(D + 1) * 4u;
 }
 
+// Fixed scratch for attn_fwd_splitkv_static: the fp32 partial O and LSE of
+// the key chunks live here instead of in a caller-supplied workspace.  It is
+// part of the module image, so every device that loads this library holds
+// ATTN_STATIC_SCRATCH_BYTES of it until the process exits.  Device code could
+// name it directly; host code must ask the runtime for its device address.
+static __device__ __align__(256) unsigned char g_static_scratch[ATTN_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices];  // device address of g_static_scratch, per device
+
+// Looks up (once per device, with that device current) where the fixed
+// scratch lives on the device.
+attn_status_t static_scratch_address(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ERR_DEVICE;
+    g_static_addr[dev] = ptr;
+  }
+  *out = g_static_addr[dev];
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1188,6 +1211,30 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
                             lse_part, st);
   if (ls != ATTN_OK) return ls;
   return launch_merge(o_part, lse_part, n_splits, rows, D, o, lse, sms, st);
+}
+
+// Key-split forward for callers that cannot allocate device memory: the
+// scratch is the fixed array above (see include/attn_fwd.h).  Nothing here
+// allocates or frees; a size beyond the fixed scratch is refused before
+// anything is launched.
+attn_status_t attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                      int S_q, int S_kv, int D, float scale, int causal,
+                                      const int32_t* kv_valid_len, int n_splits, void* stream) {
+  const attn_status_t as = check_args(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len);
+  if (as != ATTN_OK) return as;
+  if (n_splits < 1 || n_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(B) * H * S_q;
+  if (n_splits > 1 && splitkv_workspace_bytes(rows, D, n_splits) > ATTN_STATIC_SCRATCH_BYTES)
+    return ATTN_ERR_UNSUPPORTED;  // the partials would not fit in the fixed scratch
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+  const attn_status_t ps = prepare_device(dev);
+  if (ps != ATTN_OK) return ps;
+  void* scratch = nullptr;
+  const attn_status_t ss = static_scratch_address(dev, &scratch);
+  if (ss != ATTN_OK) return ss;
+  return attn_fwd_splitkv(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len, n_splits, scratch,
+                          ATTN_STATIC_SCRATCH_BYTES, stream);
 }
 
 attn_status_t attn_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t rows, int D, void* o,
