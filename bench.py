@@ -65,6 +65,11 @@ WORKLOADS = {
                                             splits="auto"),
     "b1_h8_q256_kv32768_d128_nosplit": dict(B=1, H=8, S=256, S_kv=32768, D=128, modes=(False,), seed=7,
                                             splits=1),
+    # e4m3 inputs stored at x16 with per-tensor descales 1/16 (real values N(0,1))
+    "b2_h32_s8192_d128_padded_fp8": dict(B=2, H=32, S=8192, D=128, modes=(False,), seed=5,
+                                         valid=(8192, 5000), dtype="e4m3", fp8_mult=16.0),
+    "b1_h32_s32768_d128_fp8": dict(B=1, H=32, S=32768, D=128, modes=(True, False), seed=6,
+                                   dtype="e4m3", fp8_mult=16.0),
 }
 DEFAULT_WORKLOAD = "b4_h16_s1024_d64"
 
@@ -117,15 +122,18 @@ def aggregate_ranks(flops_step, t_step_ms, t_e2e_ms, dist=None, device="cpu"):
     return total / (t_max * 1e-3) / 1e12, total / (t_e2e_max * 1e-3) / 1e12, t_max, t_e2e_max
 
 
-def load_peaks():
+def load_peaks(dtype="bf16"):
+    """Dense tensor peak for the workload's operand type.  e4m3 takes the bf16
+    figure times the nominal fp8:bf16 ratio (4.5 / 2.25 PFLOP/s = 2)."""
+    ratio, note = (2.0, " x 2 (nominal fp8:bf16 dense ratio)") if dtype == "e4m3" else (1.0, "")
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
         try:
             d = json.loads(p.read_text())
-            return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+            return ratio * float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)" + note
         except (ValueError, KeyError):
             pass
-    return FALLBACK_PEAK_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst)"
+    return ratio * FALLBACK_PEAK_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst)" + note
 
 
 def kernel_source_hash():
@@ -330,9 +338,16 @@ def main():
     S_kv = s_kv(w)
     modes = w["modes"]
     scale = 1.0 / math.sqrt(D)
-    q, k, v = si.qkv_bf16_torch(w["seed"], B, H, S, S_kv, D, w.get("q_mult", 1.0), w.get("k_mult", 1.0),
-                                device=dev)
-    o = torch.empty_like(q)
+    fp8 = w.get("dtype") == "e4m3"
+    if fp8:
+        m8 = w["fp8_mult"]
+        q, k, v = (si.normal_e4m3_torch(w["seed"], tid, B * H * n * D, m8, device=dev).view(B, H, n, D)
+                   for tid, n in ((si.TID_Q, S), (si.TID_K, S_kv), (si.TID_V, S_kv)))
+        descale = 1.0 / m8
+    else:
+        q, k, v = si.qkv_bf16_torch(w["seed"], B, H, S, S_kv, D, w.get("q_mult", 1.0), w.get("k_mult", 1.0),
+                                    device=dev)
+    o = torch.empty((B, H, S, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
     kvl = torch.tensor(w["valid"], dtype=torch.int32, device=dev) if w.get("valid") else None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -345,7 +360,10 @@ def main():
     kernels_per_call = 2 if splits > 1 else 1  # key-split calls add the merge kernel
 
     def launch(causal):
-        if splits > 1:
+        if fp8:
+            attn.attn_fwd_fp8(q, k, v, o, lse, B, H, S, S_kv, D, scale, descale, descale, descale, causal, kvl,
+                              stream)
+        elif splits > 1:
             attn.attn_fwd_splitkv(q, k, v, o, lse, B, H, S, S_kv, D, scale, causal, kvl, splits, ws, ws_bytes,
                                   stream)
         else:
@@ -424,7 +442,7 @@ def main():
     # roofline of the attention kernel: every launch in the step is attn_fwd_sm103a<D>
     mean_launch_ms = sum(sum(x) for x in launch_ms) / (args.steps * n_l)
     flops_launch = flops_step / n_l
-    peak, peak_src = load_peaks()
+    peak, peak_src = load_peaks(w.get("dtype", "bf16"))
     achieved = flops_launch / (mean_launch_ms * 1e-3) / 1e12
     per_mode = {("causal" if c else "non-causal"): {
         "ms": sum(launch_ms[j]) / args.steps,
@@ -435,8 +453,9 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 Q/K/V drawn on the device)",
+        "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "data": ("synthetic (seeded N(0,1) x16 rounded to e4m3 on the device, descale 1/16)" if fp8 else
+                 "synthetic (seeded N(0,1) bf16 Q/K/V drawn on the device)"),
         "config": {"workload": args.workload, "B": B, "H": H, "S_q": S, "S_kv": S_kv, "D": D,
                    "kv_splits": splits,
                    "scale": scale, "modes": ["causal" if c else "non-causal" for c in modes],
@@ -448,7 +467,7 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
                      "alg_bytes_per_launch": sum(alg_bytes(w, c) for c in modes) / n_l,
-                     "kernel": (f"attn_fwd_sm103a<{D}>" if splits == 1 else
+                     "kernel": (f"attn_fwd_sm103a<{D}, e4m3>" if fp8 else f"attn_fwd_sm103a<{D}>" if splits == 1 else
                                 f"attn_fwd_sm103a<{D}, split> + attn_merge_kernel<{D}> (one call, both timed)"),
                      "peak_source": peak_src},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -458,7 +477,10 @@ def main():
 
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         import numpy as np
-        hb = [x.view(torch.int16).numpy().view(np.uint16) for x in (hq, hk, hv)]
+        if fp8:  # the oracle reads the e4m3 values as bf16 (exact) with the descales folded in
+            hb = [si.e4m3_bits_to_bf16_bits(x.view(torch.uint8).numpy()) for x in (hq, hk, hv)]
+        else:
+            hb = [x.view(torch.int16).numpy().view(np.uint16) for x in (hq, hk, hv)]
         tf, dt, rows, threads = oracle_sample(w, *hb, args.cpu_seconds, modes)
         line["cpu_baseline"] = {
             "value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",

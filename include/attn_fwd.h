@@ -74,6 +74,30 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        const int32_t* kv_valid_len, void* stream);
 
 /*
+ * attn_fwd_fp8 -- attn_fwd on FP8 (e4m3) inputs, after the FP8 support the
+ * "Flash attention" glossary page names for FlashAttention-3 (paragraph 2).
+ *
+ *   q, k, v       device pointers, e4m3 bytes (1 sign, 4 exponent bits with
+ *                 bias 7, 3 mantissa bits), [B][H][S][D], 16-byte aligned.
+ *   q_descale, k_descale, v_descale
+ *                 per-tensor factors, finite and > 0: the real inputs are
+ *                 q_descale * Q8, k_descale * K8, v_descale * V8.
+ *   o, lse        as attn_fwd: bf16 O and fp32 natural-log LSE of attention
+ *                 over the real (descaled) inputs.
+ *   D             128 only (ATTN_ERR_UNSUPPORTED otherwise).
+ * S = (scale * q_descale * k_descale) * Q8.K8^T is accumulated exactly in
+ * fp32 on the tensor cores (kind::f8f6f4).  The probabilities P enter the
+ * P.V product as e4m3 (relative rounding error up to 2^-4 each), while the
+ * normaliser l sums them in fp32; O therefore carries a few per cent of
+ * relative error and LSE the same accuracy as attn_fwd.  Other arguments,
+ * limits and behaviour as attn_fwd.
+ */
+attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int S_q, int S_kv, int D, float scale, float q_descale,
+                           float k_descale, float v_descale, int causal,
+                           const int32_t* kv_valid_len, void* stream);
+
+/*
  * attn_fwd_splitkv -- the same result as attn_fwd, with the keys of every
  * query tile split into `n_splits` contiguous chunks of whole 128-key tiles
  * that are computed independently (more parallel work when B*H*ceil(S_q/256)

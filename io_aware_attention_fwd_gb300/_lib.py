@@ -20,7 +20,7 @@ ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_DEVICE = 6
 
 # every extern "C" function include/attn_fwd.h declares
-EXPORTED = ("attn_fwd", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
+EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
             "attn_fwd_splitkv_suggest", "attn_merge", "attn_fwd_splitkv_static", "attn_status_str", "attn_fwd_debug_status",
             "attn_watchdog_selftest", "attn_fwd_abi_version")
 
@@ -56,6 +56,9 @@ def load() -> ctypes.CDLL:
             lib.attn_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
             lib.attn_fwd_splitkv_suggest.restype = i
             lib.attn_fwd_splitkv_suggest.argtypes = [i, i, i, i, i, i]
+            f = ctypes.c_float
+            lib.attn_fwd_fp8.restype = i
+            lib.attn_fwd_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, f, f, f, f, i, p, p]
             lib.attn_fwd_splitkv_static.restype = i
             lib.attn_fwd_splitkv_static.argtypes = [p, p, p, p, p, i, i, i, i, i, ctypes.c_float, i, p, i, p]
             lib.attn_merge.restype = i
@@ -105,6 +108,18 @@ def attn_fwd(q, k, v, o, lse, B: int, H: int, S_q: int, S_kv: int, D: int, scale
                          _addr(kv_valid_len), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
+
+
+def attn_fwd_fp8(q, k, v, o, lse, B: int, H: int, S_q: int, S_kv: int, D: int, scale: float,
+                 q_descale: float, k_descale: float, v_descale: float, causal: bool,
+                 kv_valid_len=None, stream=None) -> None:
+    """Enqueue the FP8 (e4m3) forward pass (see include/attn_fwd.h)."""
+    st = load().attn_fwd_fp8(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), int(B), int(H),
+                             int(S_q), int(S_kv), int(D), float(scale), float(q_descale),
+                             float(k_descale), float(v_descale), int(bool(causal)),
+                             _addr(kv_valid_len), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_fp8")
 
 
 def attn_fwd_splitkv(q, k, v, o, lse, B: int, H: int, S_q: int, S_kv: int, D: int, scale: float,

@@ -69,12 +69,21 @@ constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 
-template <int D>
+// Per head dim and element type (kF8: e4m3 Q/K/V and P, else bf16).
+template <int D, bool kF8>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kPanels = D / 64;
-  static constexpr int kTileBytes = 128 * D * 2;  // one [128 x D] bf16 tile
-  static constexpr int kSlots = (D == 128) ? 5 : 12;
+  static_assert(!kF8 || D == 128, "e4m3 path: D = 128");
+  static constexpr int kEB = kF8 ? 1 : 2;             // bytes per element
+  static constexpr int kRowBytes = D * kEB;           // one Q/K/V row
+  static constexpr int kPanels = kRowBytes / 128;     // 128-byte swizzle panels per row
+  static constexpr int kBoxCols = 128 / kEB;          // elements per TMA box row
+  static constexpr int kTileBytes = 128 * kRowBytes;  // one [128 x D] tile
+  static constexpr int kQkSteps = kRowBytes / 32;     // MMA K steps of 32 bytes over D
+  static constexpr int kKeysPerStep = 32 / kEB;       // keys per P.V MMA K step
+  static constexpr int kPvSteps = kBN / kKeysPerStep;
+  static constexpr int kPCols = kBN * kEB / 4;        // TMEM columns of packed P
+  static constexpr int kSlots = kF8 ? 12 : ((D == 128) ? 5 : 12);
   static constexpr int kQOff = 0;
   static constexpr int kSlotOff = kQTiles * kTileBytes;
   static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
@@ -101,6 +110,7 @@ struct Params {
   float scale_log2;      // scale * log2(e)
   int causal;
   unsigned long long timeout_ns;
+  float o_scale;          // multiplies O (the V descale of the e4m3 path, else 1)
   float* o_part;         // split mode: fp32 [n_splits][BH * S_q][D]
   float* lse_part;       // split mode: fp32 [n_splits][BH * S_q]
 };
@@ -243,26 +253,50 @@ __device__ __forceinline__ void tc_commit_if(uint32_t pred, uint32_t bar) {
       : "memory");
 }
 
-// The same MMAs as below, issued only when `pred` is set (the elected lane).
+// D[tmem] (+)= A . B on the tensor core, issued only when `pred` is set (the
+// elected lane).  SS: A and B from shared memory; TS: A from tensor memory.
+// kind::f16 for bf16 operands, kind::f8f6f4 for e4m3 operands.
+template <bool kF8>
 __device__ __forceinline__ void mma_ss_if(uint32_t pred, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.ne.b32 q, %5, 0;\n\t"
-      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
-      : "memory");
+  if constexpr (kF8) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+        : "memory");
+  }
 }
+template <bool kF8>
 __device__ __forceinline__ void mma_ts_if(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.ne.b32 q, %5, 0;\n\t"
-      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
-      : "memory");
+  if constexpr (kF8) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+        : "memory");
+  }
 }
 
 #define ATTN_R32(i) "=r"(r[(i)])
@@ -313,13 +347,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Four fp32 -> e4m3 (round to nearest even, saturating), element i in byte i.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float p0, float p1, float p2, float p3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(p1), "f"(p0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(p3), "f"(p2));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
 // --- descriptors -----------------------------------------------------------
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor, fp32 accumulator, M x N.  kind::f16 with bf16 A and
+// B (format code 1), or kind::f8f6f4 with e4m3 A and B (format code 0).
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn_major, bool b_mn_major, bool e4m3) {
   return (1u << 4)                                 // D format: f32
-         | (1u << 7)                               // A format: bf16
-         | (1u << 10)                              // B format: bf16
+         | ((e4m3 ? 0u : 1u) << 7)                 // A format
+         | ((e4m3 ? 0u : 1u) << 10)                // B format
          | ((a_mn_major ? 1u : 0u) << 15)          // A major-ness
          | ((b_mn_major ? 1u : 0u) << 16)          // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
@@ -344,29 +387,33 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t addr, uint32_t 
          (static_cast<uint64_t>(2) << 61);
 }
 
-// S[tmem] = Q_tile[smem] . K_tile[smem]^T over the head dim (K = D, 16 per MMA).
-// qd/kd are the tiles' base descriptors; a step of k elements within a
-// 128-byte swizzle row adds 32 bytes (2 in the 16-byte address field), and
-// the next 64-column panel adds kPanelBytes.  Addresses stay below 256 KB, so
-// the 14-bit field never carries.
-template <int D>
+// S[tmem] = Q_tile[smem] . K_tile[smem]^T over the head dim; every MMA
+// consumes 32 bytes of each row (16 bf16 or 32 e4m3 elements).  qd/kd are the
+// tiles' base descriptors; a step within a 128-byte swizzle row adds 32 bytes
+// (2 in the 16-byte address field), and the next 128-byte panel adds
+// kPanelBytes.  Addresses stay below 256 KB, so the 14-bit field never
+// carries.
+template <int D, bool kF8>
 __device__ __forceinline__ void issue_qk(uint32_t pred, uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc) {
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
+  for (int kk = 0; kk < Cfg<D, kF8>::kQkSteps; ++kk) {
     const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
-    mma_ss_if(pred, d_tmem, qd + off, kd + off, idesc, kk > 0 ? 1u : 0u);
+    mma_ss_if<kF8>(pred, d_tmem, qd + off, kd + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// O[tmem] (+)= P[tmem] . V_tile[smem] over the keys (K = 128, 16 per MMA); a
-// step of 16 keys is 16 rows of 128 bytes in the MN-major V layout.
-template <int D>
+// O[tmem] (+)= P[tmem] . V_tile[smem] over the 128 keys; every MMA consumes 32
+// bytes of each P row (8 TMEM columns) and kKeysPerStep rows of 128 bytes of
+// the MN-major V layout.
+template <int D, bool kF8>
 __device__ __forceinline__ void issue_pv(uint32_t pred, uint32_t d_tmem, uint32_t p_tmem, uint64_t vd, uint32_t idesc,
                                          bool accumulate) {
+  using C = Cfg<D, kF8>;
 #pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk) {
-    mma_ts_if(pred, d_tmem, p_tmem + static_cast<uint32_t>(kk * 8), vd + static_cast<uint64_t>((kk * 16 * 128) >> 4),
-              idesc, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < C::kPvSteps; ++kk) {
+    mma_ts_if<kF8>(pred, d_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+                   vd + static_cast<uint64_t>((kk * C::kKeysPerStep * 128) >> 4), idesc,
+                   (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -402,20 +449,20 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
 // Work units and shared-memory map
 // ---------------------------------------------------------------------------
 
-template <int D>
+template <int D, bool kF8>
 struct Smem {
   uint32_t base;  // shared address, 1024-aligned
-  __device__ uint32_t q(int t) const { return base + Cfg<D>::kQOff + t * Cfg<D>::kTileBytes; }
-  __device__ uint32_t slot(int s) const { return base + Cfg<D>::kSlotOff + s * Cfg<D>::kTileBytes; }
-  __device__ uint32_t bar(int i) const { return base + Cfg<D>::kBarOff + 8 * i; }
+  __device__ uint32_t q(int t) const { return base + Cfg<D, kF8>::kQOff + t * Cfg<D, kF8>::kTileBytes; }
+  __device__ uint32_t slot(int s) const { return base + Cfg<D, kF8>::kSlotOff + s * Cfg<D, kF8>::kTileBytes; }
+  __device__ uint32_t bar(int i) const { return base + Cfg<D, kF8>::kBarOff + 8 * i; }
   __device__ uint32_t bar_q() const { return bar(0); }
   __device__ uint32_t bar_qfree(int t) const { return bar(1 + t); }
   __device__ uint32_t bar_full(int s) const { return bar(1 + kQTiles + s); }
-  __device__ uint32_t bar_empty(int s) const { return bar(1 + kQTiles + Cfg<D>::kSlots + s); }
-  __device__ uint32_t bar_s(int t) const { return bar(1 + kQTiles + 2 * Cfg<D>::kSlots + t); }
-  __device__ uint32_t bar_p(int t) const { return bar(1 + 2 * kQTiles + 2 * Cfg<D>::kSlots + t); }
-  __device__ uint32_t bar_o(int t) const { return bar(1 + 3 * kQTiles + 2 * Cfg<D>::kSlots + t); }
-  __device__ uint32_t bar_drain() const { return bar(1 + 4 * kQTiles + 2 * Cfg<D>::kSlots); }
+  __device__ uint32_t bar_empty(int s) const { return bar(1 + kQTiles + Cfg<D, kF8>::kSlots + s); }
+  __device__ uint32_t bar_s(int t) const { return bar(1 + kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
+  __device__ uint32_t bar_p(int t) const { return bar(1 + 2 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
+  __device__ uint32_t bar_o(int t) const { return bar(1 + 3 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
+  __device__ uint32_t bar_drain() const { return bar(1 + 4 * kQTiles + 2 * Cfg<D, kF8>::kSlots); }
 };
 
 // One work unit: two 128-row query tiles of one (batch, head).
@@ -501,10 +548,10 @@ __device__ __forceinline__ int unit_of(int r, int c, int G) { return r * G + ((r
 
 // TMA producer (one thread).  Per unit: Q_0, Q_1, then K_0, V_0, K_1, V_1, ...;
 // K/V item `it` (counted across units) lives in slot it % kSlots.
-template <int D>
-__device__ void load_role(const Smem<D>& sm, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+template <int D, bool kF8>
+__device__ void load_role(const Smem<D, kF8>& sm, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                           const CUtensorMap* tmV, const Params& p, const WaitCtx& w) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kF8>;
   tma_prefetch_desc(tmQ);
   tma_prefetch_desc(tmK);
   tma_prefetch_desc(tmV);
@@ -526,7 +573,7 @@ __device__ void load_role(const Smem<D>& sm, const CUtensorMap* tmQ, const CUten
       int y = un.q0 + t * kBM;
       if (y >= p.S_q) y = un.q0;  // a tile wholly past the end reloads tile 0 (never stored)
       for (int pn = 0; pn < C::kPanels; ++pn)
-        tma_load_3d(sm.q(t) + pn * kPanelBytes, tmQ, sm.bar_q(), pn * 64, y, un.bh);
+        tma_load_3d(sm.q(t) + pn * kPanelBytes, tmQ, sm.bar_q(), pn * C::kBoxCols, y, un.bh);
     }
     ++k;
     for (int j = 0; j < un.n && ok; ++j) {
@@ -540,7 +587,7 @@ __device__ void load_role(const Smem<D>& sm, const CUtensorMap* tmQ, const CUten
         mbar_expect_tx(sm.bar_full(s), C::kTileBytes);
         const CUtensorMap* m = kv ? tmV : tmK;
         for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_3d(sm.slot(s) + pn * kPanelBytes, m, sm.bar_full(s), pn * 64, (un.j0 + j) * kBN, un.bh);
+          tma_load_3d(sm.slot(s) + pn * kPanelBytes, m, sm.bar_full(s), pn * C::kBoxCols, (un.j0 + j) * kBN, un.bh);
         ++it;
       }
     }
@@ -559,11 +606,11 @@ __device__ void load_role(const Smem<D>& sm, const CUtensorMap* tmQ, const CUten
 // The first P_t V of a unit overwrites O_t only after P_t of that unit is
 // ready, which the softmax warps signal after they have read the previous
 // unit's O_t out of TMEM.
-template <int D>
-__device__ void mma_role(const Smem<D>& sm, uint32_t tmem, const Params& p, const WaitCtx& w) {
-  using C = Cfg<D>;
-  constexpr uint32_t idesc_s = make_idesc_bf16(kBM, kBN, false, false);
-  constexpr uint32_t idesc_pv = make_idesc_bf16(kBM, D, false, true);
+template <int D, bool kF8>
+__device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p, const WaitCtx& w) {
+  using C = Cfg<D, kF8>;
+  constexpr uint32_t idesc_s = make_idesc(kBM, kBN, false, false, kF8);
+  constexpr uint32_t idesc_pv = make_idesc(kBM, D, false, true, kF8);
   const uint32_t leader = elect_one();
   const uint32_t tS[kQTiles] = {tmem, tmem + kBN};
   const uint32_t tO[kQTiles] = {tmem + C::kOCol0, tmem + C::kOCol0 + D};
@@ -588,7 +635,7 @@ __device__ void mma_role(const Smem<D>& sm, uint32_t tmem, const Params& p, cons
     tc_fence_after();
 #pragma unroll
     for (int t = 0; t < kQTiles; ++t) {  // S_t = Q_t K_0^T (S_t is free: the last P_t V was issued before)
-      issue_qk<D>(leader, tS[t], qd[t], kd0 + sk0 * kSlotStep, idesc_s);
+      issue_qk<D, kF8>(leader, tS[t], qd[t], kd0 + sk0 * kSlotStep, idesc_s);
       tc_commit_if(leader, sm.bar_s(t));
       if (un.nkv[t] == 1) tc_commit_if(leader, sm.bar_qfree(t));
     }
@@ -608,10 +655,10 @@ __device__ void mma_role(const Smem<D>& sm, uint32_t tmem, const Params& p, cons
         ++pc[t];
         if (!ok) continue;
         tc_fence_after();
-        issue_pv<D>(leader, tO[t], tS[t], vd0 + sv * kSlotStep, idesc_pv, j > 0);
+        issue_pv<D, kF8>(leader, tO[t], tS[t], vd0 + sv * kSlotStep, idesc_pv, j > 0);
         tc_commit_if(leader, sm.bar_o(t));
         if (j + 1 < un.nkv[t]) {
-          issue_qk<D>(leader, tS[t], qd[t], kd0 + skn * kSlotStep, idesc_s);
+          issue_qk<D, kF8>(leader, tS[t], qd[t], kd0 + skn * kSlotStep, idesc_s);
           tc_commit_if(leader, sm.bar_s(t));
           if (j + 2 == un.nkv[t]) tc_commit_if(leader, sm.bar_qfree(t));
         }
@@ -634,9 +681,9 @@ __device__ void mma_role(const Smem<D>& sm, uint32_t tmem, const Params& p, cons
 
 // Softmax + epilogue for query tile t (128 threads, one query row each).
 // kSplit: the unit covers one key chunk and writes fp32 O and LSE partials.
-template <int D, bool kSplit>
-__device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Params& p, const WaitCtx& w) {
-  using C = Cfg<D>;
+template <int D, bool kSplit, bool kF8>
+__device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const Params& p, const WaitCtx& w) {
+  using C = Cfg<D, kF8>;
   const int r = static_cast<int>(threadIdx.x) - kBM * (1 + t);  // row in tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_off + t * kBN;
@@ -698,20 +745,33 @@ __device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Para
 
       // p = 2^(s*c - m): one FFMA and one MUFU.EX2 per score; the fp32 p
       // feed the row sum, their bf16 pairs feed the P.V MMA.
-      uint32_t pk[kBN / 2];
+      uint32_t pk[C::kPCols];
       float sum0 = 0.f, sum1 = 0.f;
+      if constexpr (kF8) {  // P as e4m3, four per TMEM column
 #pragma unroll
-      for (int i = 0; i < kBN / 2; ++i) {
-        const float a = ex2_approx(fmaf(s[2 * i], c, -mc));
-        const float b = ex2_approx(fmaf(s[2 * i + 1], c, -mc));
-        sum0 += a;
-        sum1 += b;
-        pk[i] = pack_bf16x2(a, b);
+        for (int i = 0; i < kBN / 4; ++i) {
+          const float a = ex2_approx(fmaf(s[4 * i], c, -mc));
+          const float b = ex2_approx(fmaf(s[4 * i + 1], c, -mc));
+          const float e = ex2_approx(fmaf(s[4 * i + 2], c, -mc));
+          const float f = ex2_approx(fmaf(s[4 * i + 3], c, -mc));
+          sum0 += a + e;
+          sum1 += b + f;
+          pk[i] = pack_e4m3x4(a, b, e, f);
+        }
+      } else {  // P as bf16, two per TMEM column
+#pragma unroll
+        for (int i = 0; i < kBN / 2; ++i) {
+          const float a = ex2_approx(fmaf(s[2 * i], c, -mc));
+          const float b = ex2_approx(fmaf(s[2 * i + 1], c, -mc));
+          sum0 += a;
+          sum1 += b;
+          pk[i] = pack_bf16x2(a, b);
+        }
       }
       const float sa = sum0, sb = sum1;
       l = l * alpha + (sa + sb);
-      tmem_st32(tS + 0, pk + 0);
-      tmem_st32(tS + 32, pk + 32);
+#pragma unroll
+      for (int cc = 0; cc < C::kPCols; cc += 32) tmem_st32(tS + cc, pk + cc);
       tmem_wait_st();
 
       // Lazy correction: O is rescaled only when some row's max grew by > 2^8.
@@ -752,7 +812,7 @@ __device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Para
     if (have_o) tc_fence_after();
     float inv_l = 0.f, lse = -INFINITY;
     if (l > 0.f) {
-      inv_l = 1.f / l;
+      inv_l = p.o_scale / l;  // o_scale: the V descale of the e4m3 path, else 1
       lse = (m_c + log2f(l)) * kLn2;
     }
     const int64_t grow = static_cast<int64_t>(un.bh) * p.S_q + row;
@@ -810,16 +870,16 @@ __device__ void softmax_role(const Smem<D>& sm, int t, uint32_t tmem, const Para
   }
 }
 
-template <int D, bool kSplit>
+template <int D, bool kSplit, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kF8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const Smem<D> sm{base};
+  const Smem<D, kF8> sm{base};
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -852,11 +912,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx w{p.timeout_ns, misc + 1};
 
   if (warp == 0) {
-    if (lane == 0) load_role<D>(sm, &tmQ, &tmK, &tmV, p, w);
+    if (lane == 0) load_role<D, kF8>(sm, &tmQ, &tmK, &tmV, p, w);
   } else if (warp == 1) {
-    mma_role<D>(sm, tmem, p, w);
+    mma_role<D, kF8>(sm, tmem, p, w);
   } else if (warp >= 4) {
-    softmax_role<D, kSplit>(sm, (warp - 4) >> 2, tmem, p, w);
+    softmax_role<D, kSplit, kF8>(sm, (warp - 4) >> 2, tmem, p, w);
   }
 
   tc_fence_before();
@@ -970,13 +1030,15 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
-// [BH][S][D] bf16 as a 3-D tensor map with 64 x 128 x 1 boxes, 128-byte swizzle.
-bool encode_3d(CUtensorMap* m, const void* ptr, int D, int S, int64_t BH) {
+// [BH][S][D] as a 3-D tensor map with (128 bytes of D) x 128 x 1 boxes and
+// 128-byte swizzle; elements are bf16 (eb = 2) or e4m3 bytes (eb = 1).
+bool encode_3d(CUtensorMap* m, const void* ptr, int D, int S, int64_t BH, int eb = 2) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * eb, static_cast<cuuint64_t>(S) * D * eb};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+  return g_encode(m, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                  const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1001,14 +1063,16 @@ attn_status_t prepare_device(int dev) {
     g_dev_state[dev].store(2, std::memory_order_release);
     return ATTN_ERR_UNSUPPORTED;
   }
-  if (cudaFuncSetAttribute(attn_fwd_sm103a<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<64>::kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_sm103a<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<128>::kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_sm103a<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<64>::kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_sm103a<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<128>::kSmemBytes) != cudaSuccess)
+  if (cudaFuncSetAttribute(attn_fwd_sm103a<64, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<64, false>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a<128, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128, false>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a<64, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<64, false>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a<128, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128, false>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a<128, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128, true>::kSmemBytes) != cudaSuccess)
     return ATTN_ERR_DEVICE;
   g_dev_sms[dev].store(std::max(1, sms), std::memory_order_relaxed);
   g_dev_state[dev].store(1, std::memory_order_release);
@@ -1018,14 +1082,17 @@ attn_status_t prepare_device(int dev) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Launches the attention kernel; with n_splits > 1 it writes fp32 partials to
-// o_part / lse_part instead of o / lse.
-template <int D>
+// o_part / lse_part instead of o / lse.  kF8: e4m3 Q, K, V; `scale` then
+// already includes the Q and K descales and o_scale is the V descale.
+template <int D, bool kF8>
 attn_status_t launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int S_q,
                      int S_kv, float scale, int causal, const int32_t* kv_valid_len, int sms, int n_splits,
-                     float* o_part, float* lse_part, cudaStream_t stream) {
+                     float* o_part, float* lse_part, cudaStream_t stream, float o_scale = 1.f) {
+  using C = Cfg<D, kF8>;
   const int64_t BH = static_cast<int64_t>(B) * H;
   CUtensorMap tq, tk, tv;
-  if (!encode_3d(&tq, q, D, S_q, BH) || !encode_3d(&tk, k, D, S_kv, BH) || !encode_3d(&tv, v, D, S_kv, BH))
+  if (!encode_3d(&tq, q, D, S_q, BH, C::kEB) || !encode_3d(&tk, k, D, S_kv, BH, C::kEB) ||
+      !encode_3d(&tv, v, D, S_kv, BH, C::kEB))
     return ATTN_ERR_LAUNCH;
   Params prm;
   prm.o = static_cast<uint16_t*>(o);
@@ -1041,13 +1108,16 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   prm.causal = causal;
   prm.timeout_ns = kDefaultTimeoutNs;
+  prm.o_scale = o_scale;
   prm.o_part = o_part;
   prm.lse_part = lse_part;
   const int grid = std::min(prm.n_units, sms);  // persistent: at most one CTA per SM
-  if (n_splits > 1)
-    attn_fwd_sm103a<D, true><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  if constexpr (kF8)
+    attn_fwd_sm103a<D, false, true><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  else if (n_splits > 1)
+    attn_fwd_sm103a<D, true, false><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
   else
-    attn_fwd_sm103a<D, false><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    attn_fwd_sm103a<D, false, false><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
@@ -1153,8 +1223,36 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   if (!get_encoder()) return ATTN_ERR_DEVICE;
   const int sms = g_dev_sms[dev].load(std::memory_order_relaxed);
   if (D == 64)
-    return launch<64>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, 1, nullptr, nullptr, st);
-  return launch<128>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, 1, nullptr, nullptr, st);
+    return launch<64, false>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, 1, nullptr, nullptr, st);
+  return launch<128, false>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, 1, nullptr, nullptr, st);
+}
+
+attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                           int S_q, int S_kv, int D, float scale, float q_descale, float k_descale, float v_descale,
+                           int causal, const int32_t* kv_valid_len, void* stream) {
+  const attn_status_t as = check_args(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len);
+  if (as != ATTN_OK) return as;
+  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  for (const float d : {q_descale, k_descale, v_descale})
+    if (!std::isfinite(d) || !(d > 0.f)) return ATTN_ERR_INVALID_ARG;
+  const double s_all = static_cast<double>(scale) * q_descale * k_descale;  // S = s_all * (Q8 . K8)
+  if (!(s_all > 0.0) || !std::isfinite(static_cast<float>(s_all)) || static_cast<float>(s_all) == 0.f)
+    return ATTN_ERR_INVALID_ARG;
+  if (S_q == 0) return ATTN_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+  const attn_status_t ps = prepare_device(dev);
+  if (ps != ATTN_OK) return ps;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (S_kv == 0) {
+    const int64_t rows = static_cast<int64_t>(B) * H * S_q;
+    const int64_t blocks = std::min<int64_t>((rows + 255) / 256, 4096);
+    attn_fill_empty<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<uint16_t*>(o), lse, rows, D);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  }
+  if (!get_encoder()) return ATTN_ERR_DEVICE;
+  return launch<128, true>(q, k, v, o, lse, B, H, S_q, S_kv, static_cast<float>(s_all), causal, kv_valid_len,
+                           g_dev_sms[dev].load(std::memory_order_relaxed), 1, nullptr, nullptr, st, v_descale);
 }
 
 uint64_t attn_fwd_splitkv_workspace_bytes(int B, int H, int S_q, int D, int n_splits) {
@@ -1205,9 +1303,9 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = o_part + static_cast<int64_t>(n_splits) * rows * D;
   const attn_status_t ls =
-      D == 64 ? launch<64>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, n_splits, o_part,
+      D == 64 ? launch<64, false>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, n_splits, o_part,
                            lse_part, st)
-              : launch<128>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, n_splits, o_part,
+              : launch<128, false>(q, k, v, o, lse, B, H, S_q, S_kv, scale, causal, kv_valid_len, sms, n_splits, o_part,
                             lse_part, st);
   if (ls != ATTN_OK) return ls;
   return launch_merge(o_part, lse_part, n_splits, rows, D, o, lse, sms, st);

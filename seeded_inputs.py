@@ -219,3 +219,90 @@ def qkv_bf16_torch(seed: int, B: int, H: int, S_q: int, S_kv: int, D: int,
     k = normal_bf16_torch(seed, TID_K, B * H * S_kv * D, k_mult, device).view(B, H, S_kv, D)
     v = normal_bf16_torch(seed, TID_V, B * H * S_kv * D, 1.0, device).view(B, H, S_kv, D)
     return q, k, v
+
+
+# --- e4m3 (FP8) inputs ---------------------------------------------------------
+#
+# e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 holds
+# the subnormals m * 2^-9; the largest finite magnitude is 448 and code 0x7F
+# (with either sign) is NaN.  Every e4m3 value is exactly a bf16 value, so the
+# bf16 oracle sees the e4m3 inputs without rounding.
+
+def _e4m3_magnitudes() -> np.ndarray:
+    vals = np.empty(128, dtype=np.float64)
+    for code in range(128):
+        e, m = code >> 3, code & 7
+        vals[code] = m * 2.0 ** -9 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    vals[127] = np.nan
+    return vals
+
+
+E4M3_MAGNITUDES = _e4m3_magnitudes()  # codes 0..126 finite and increasing
+E4M3_MAX = 448.0
+
+
+def f64_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest e4m3 value (ties to even code), saturating at +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    t = E4M3_MAGNITUDES[:127]
+    hi = np.clip(np.searchsorted(t, a), 1, 126)
+    lo = hi - 1
+    d_lo = a - t[lo]
+    d_hi = t[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return code | (np.signbit(x).astype(np.uint8) << np.uint8(7))
+
+
+def e4m3_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen e4m3 codes to float32 exactly."""
+    bits = np.asarray(bits, dtype=np.uint8)
+    mag = E4M3_MAGNITUDES[bits & np.uint8(0x7F)]
+    return np.where(bits & np.uint8(0x80), -mag, mag).astype(np.float32)
+
+
+def e4m3_bits_to_bf16_bits(bits: np.ndarray) -> np.ndarray:
+    """The same values as bf16 bit patterns (exact: e4m3 is a subset of bf16)."""
+    return f32_to_bf16_bits(e4m3_bits_to_f32(bits))
+
+
+def normal_e4m3(seed: int, tensor_id: int, count: int, multiplier: float = 1.0) -> np.ndarray:
+    """``count`` draws of N(0,1) * multiplier rounded to e4m3 (uint8 codes)."""
+    out = np.empty(count, dtype=np.uint8)
+    for lo in range(0, count, _CHUNK):
+        n = min(_CHUNK, count - lo)
+        out[lo:lo + n] = f64_to_e4m3_bits(normal_f64(seed, tensor_id, n, start=lo) * multiplier)
+    return out
+
+
+def qkv_e4m3(seed: int, B: int, H: int, S_q: int, S_kv: int, D: int,
+             mults=(1.0, 1.0, 1.0)):
+    """Q, K, V as e4m3 codes [B,H,S,D]; element = round(N(0,1) * mult)."""
+    q = normal_e4m3(seed, TID_Q, B * H * S_q * D, mults[0]).reshape(B, H, S_q, D)
+    k = normal_e4m3(seed, TID_K, B * H * S_kv * D, mults[1]).reshape(B, H, S_kv, D)
+    v = normal_e4m3(seed, TID_V, B * H * S_kv * D, mults[2]).reshape(B, H, S_kv, D)
+    return q, k, v
+
+
+def normal_e4m3_torch(seed: int, tensor_id: int, count: int, multiplier: float = 1.0, device="cuda",
+                      chunk: int = 1 << 25):
+    """Device version for the benchmark: the same normals, rounded through
+    float32 to torch.float8_e4m3fn (a float32 tie can round differently from
+    the host's direct rounding in rare cases; parity tests draw on the host)."""
+    import torch
+
+    out = torch.empty(count, dtype=torch.float8_e4m3fn, device=device)
+    for lo in range(0, count, chunk):
+        n = min(chunk, count - lo)
+        # the bf16 draw holds the same float64 normal rounded twice; redo it in float32
+        npairs = (n + 1) // 2
+        s0 = _mix64_int(seed * 0x9E3779B97F4A7C15 + tensor_id)
+        idx = torch.arange(lo + 1, lo + 2 * npairs + 1, dtype=torch.int64, device=device)
+        w = _mix64_t(idx * _to_i64(0x9E3779B97F4A7C15) + _to_i64(s0))
+        u = (_lsr_t(w, 11).to(torch.float64) + 0.5) * (2.0 ** -53)
+        r = torch.sqrt(-2.0 * torch.log(u[0::2]))
+        th = (2.0 * math.pi) * u[1::2]
+        z = torch.stack([r * torch.cos(th), r * torch.sin(th)], dim=1).reshape(-1)[:n] * multiplier
+        out[lo:lo + n] = z.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float32).to(torch.float8_e4m3fn)
+    return out

@@ -146,3 +146,19 @@ def test_merge_argument_checks(kw, expect):
     args = dict(o_parts=FAKE, lse_parts=FAKE, n_parts=3, rows=100, D=64, o=FAKE, lse=FAKE)
     args.update(kw)
     assert attn.call_status(attn.attn_merge, **args) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(D=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(q_descale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k_descale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(v_descale=-1.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=1e-30, q_descale=1e-30, k_descale=1e-30), attn.ATTN_ERR_INVALID_ARG),  # underflows
+    (dict(q=FAKE + 4), attn.ATTN_ERR_ALIGNMENT),
+    (dict(S_q=0), attn.ATTN_OK),
+])
+def test_fp8_argument_checks(kw, expect):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=2, S_q=128, S_kv=128, D=128,
+                scale=0.1, q_descale=1.0, k_descale=1.0, v_descale=1.0, causal=False)
+    args.update(kw)
+    assert attn.call_status(attn.attn_fwd_fp8, **args) == expect

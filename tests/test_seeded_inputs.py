@@ -73,3 +73,31 @@ def test_torch_generator_matches_host_generator():
     # any difference is a single bf16 step
     diff = np.abs(host.astype(np.int32) - dev_bits.astype(np.int32))
     assert diff.max() <= 1
+
+
+def test_e4m3_table_and_rounding():
+    t = si.E4M3_MAGNITUDES
+    assert t[1] == 2.0 ** -9 and t[8] == 2.0 ** -6 and t[126] == 448.0 and np.isnan(t[127])
+    assert np.all(np.diff(t[:127]) > 0)
+    # ties go to the even code; saturation at 448; sign bit
+    mid = (t[9] + t[10]) / 2          # between codes 9 and 10 -> 10
+    assert si.f64_to_e4m3_bits(np.array([mid]))[0] == 10
+    mid = (t[10] + t[11]) / 2         # between 10 and 11 -> 10
+    assert si.f64_to_e4m3_bits(np.array([mid]))[0] == 10
+    assert list(si.f64_to_e4m3_bits(np.array([1e6, -1e6, -0.0, 2.0 ** -11]))) == [126, 254, 128, 0]
+    x = np.array([1.0, -2.5, 0.0137, 300.0])
+    back = si.e4m3_bits_to_f32(si.f64_to_e4m3_bits(x))
+    assert list(back) == [1.0, -2.5, 0.013671875, 288.0]
+
+
+def test_e4m3_matches_torch_cast_and_widens_exactly_to_bf16():
+    torch = __import__("pytest").importorskip("torch")
+    x = si.normal_f64(8, 1, 100_000) * 37.0
+    x = np.clip(x, -448, 448)
+    ours = si.f64_to_e4m3_bits(x)
+    theirs = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, theirs)
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]
+    f32 = si.e4m3_bits_to_f32(codes)
+    assert np.array_equal(si.bf16_bits_to_f32(si.e4m3_bits_to_bf16_bits(codes)), f32)
