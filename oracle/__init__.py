@@ -61,6 +61,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.attn_ref_score_buffer_bytes.argtypes = [i64, i64, i64, i64]
     lib.attn_ref_hardware_threads.restype = ctypes.c_int
     lib.attn_ref_hardware_threads.argtypes = []
+    lib.attn_ref_f64_dbl.restype = ctypes.c_int
+    lib.attn_ref_f64_dbl.argtypes = lib.attn_ref_f64.argtypes
     return lib
 
 
@@ -108,6 +110,78 @@ def attention_f64(q_bits, k_bits, v_bits, scale: float, causal: bool,
     if rc != 0:
         raise ValueError(f"attn_ref_f64 rejected its arguments (rc={rc})")
     return o, lse
+
+
+def attention_f64_dbl(q, k, v, scale: float, causal: bool, kv_valid_len=None, rows=None,
+                      threads: int = 0, lib=None):
+    """attention_f64 on float64 inputs (same layouts), through the same C++ code."""
+    lib = lib or load_library()
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    B, H, S_q, D = q.shape
+    S_kv = k.shape[2]
+    kvl = None if kv_valid_len is None else np.ascontiguousarray(kv_valid_len, dtype=np.int32)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n_rows = B * H * S_q if r is None else int(r.shape[0])
+    o = np.empty((n_rows, D), dtype=np.float64)
+    lse = np.empty((n_rows,), dtype=np.float64)
+    rc = lib.attn_ref_f64_dbl(_ptr(q), _ptr(k), _ptr(v), B, H, S_q, S_kv, D, float(scale),
+                              int(bool(causal)), _ptr(kvl), _ptr(r), n_rows, _ptr(o), _ptr(lse),
+                              int(threads))
+    if rc != 0:
+        raise ValueError(f"attn_ref_f64_dbl rejected its arguments (rc={rc})")
+    return o, lse
+
+
+def _widen(x):
+    x = np.asarray(x)
+    if x.dtype == np.uint16:  # bf16 bit patterns
+        return (x.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def attention_bwd_f64(q, k, v, d_o, scale: float, causal: bool, kv_valid_len=None):
+    """Gradients of the attention forward pass, in float64.
+
+    q, d_o: [B,H,S_q,D]; k, v: [B,H,S_kv,D], as bf16 bit patterns (uint16) or
+    float arrays.  For each (b, h), with the masked score matrix
+    S = scale * Q K^T (masked entries -inf) and P = softmax(S) row by row (a
+    row with no allowed key is all zero):
+        dV = P^T dO,  dP = dO V^T,  dS = P * (dP - rowsum(P * dP)),
+        dQ = scale * dS K,  dK = scale * dS^T Q.
+    These are the chain rule through O = P V and the softmax; the forward
+    pass is the one the pages define ("Attention memory" page, "What this
+    memory is"; masked keys as in the masked_fill sentences of the "PyTorch
+    attention backends" story).  P is materialised per head: plain, slow,
+    obviously correct.  Returns (dq, dk, dv) as float64 arrays.
+    """
+    q, k, v, d_o = (_widen(x) for x in (q, k, v, d_o))
+    B, H, S_q, D = q.shape
+    S_kv = k.shape[2]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    i = np.arange(S_q)[:, None]
+    j = np.arange(S_kv)[None, :]
+    for b in range(B):
+        valid = S_kv if kv_valid_len is None else min(max(int(kv_valid_len[b]), 0), S_kv)
+        allowed = np.broadcast_to(j < valid, (S_q, S_kv))
+        if causal:
+            allowed = allowed & (j <= i)
+        for h in range(H):
+            s = scale * (q[b, h] @ k[b, h].T)
+            s = np.where(allowed, s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            e = np.where(allowed, np.exp(s - np.where(np.isfinite(m), m, 0.0)), 0.0)
+            l = e.sum(axis=1, keepdims=True)
+            p = np.divide(e, l, out=np.zeros_like(e), where=l > 0)
+            dv[b, h] = p.T @ d_o[b, h]
+            dp = d_o[b, h] @ v[b, h].T
+            ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+            dq[b, h] = scale * (ds @ k[b, h])
+            dk[b, h] = scale * (ds.T @ q[b, h])
+    return dq, dk, dv
 
 
 def score_buffer_bytes(B: int, H: int, s: int, e: int, lib=None) -> int:

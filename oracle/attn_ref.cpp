@@ -23,8 +23,8 @@
 //   * "Attention memory" page, sections "Formula" and "Worked example": the
 //     materialised score buffer holds B * H * s^2 * e bytes.
 //
-// Inputs are bf16 bit patterns, widened exactly to double.  Every product and
-// sum is in double.
+// Inputs are bf16 bit patterns widened exactly to double (or, through
+// attn_ref_f64_dbl, doubles).  Every product and sum is in double.
 //
 // Parity pins: tests/test_oracle_pins.py (worked-example bytes, row sums,
 // constant V, Q = 0, causal row 0, key permutation, padding = truncation,
@@ -49,10 +49,15 @@ double bf16_to_double(uint16_t bits) {
   return static_cast<double>(f);
 }
 
+// Inputs either as bf16 bit patterns or as doubles (the latter lets the tests
+// take finite differences of the forward pass).
 struct Problem {
   const uint16_t* q;
   const uint16_t* k;
   const uint16_t* v;
+  const double* qd;  // when non-null, q/k/v are read from qd/kd/vd instead
+  const double* kd;
+  const double* vd;
   int64_t B, H, S_q, S_kv, D;
   double scale;
   int causal;
@@ -70,15 +75,19 @@ bool key_allowed(const Problem& p, int64_t b, int64_t i, int64_t j) {
   return true;
 }
 
+double q_at(const Problem& p, int64_t idx) { return p.qd ? p.qd[idx] : bf16_to_double(p.q[idx]); }
+double k_at(const Problem& p, int64_t idx) { return p.kd ? p.kd[idx] : bf16_to_double(p.k[idx]); }
+double v_at(const Problem& p, int64_t idx) { return p.vd ? p.vd[idx] : bf16_to_double(p.v[idx]); }
+
 // One output row: materialise the score row, then a two-pass softmax.
 void one_row(const Problem& p, int64_t flat_row, double* o_row, double* lse_out,
              std::vector<double>& s_row) {
   const int64_t b = flat_row / (p.H * p.S_q);
   const int64_t h = (flat_row / p.S_q) % p.H;
   const int64_t i = flat_row % p.S_q;
-  const uint16_t* qi = p.q + ((b * p.H + h) * p.S_q + i) * p.D;
-  const uint16_t* kbh = p.k + (b * p.H + h) * p.S_kv * p.D;
-  const uint16_t* vbh = p.v + (b * p.H + h) * p.S_kv * p.D;
+  const int64_t qi = ((b * p.H + h) * p.S_q + i) * p.D;   // element offsets
+  const int64_t kbh = (b * p.H + h) * p.S_kv * p.D;
+  const int64_t vbh = kbh;
   const double neg_inf = -std::numeric_limits<double>::infinity();
 
   // Scores s_ij = scale * q_i . k_j, with masked entries set to -inf.
@@ -87,7 +96,7 @@ void one_row(const Problem& p, int64_t flat_row, double* o_row, double* lse_out,
     if (!key_allowed(p, b, i, j)) continue;
     double dot = 0.0;
     for (int64_t d = 0; d < p.D; ++d) {
-      dot += bf16_to_double(qi[d]) * bf16_to_double(kbh[j * p.D + d]);
+      dot += q_at(p, qi + d) * k_at(p, kbh + j * p.D + d);
     }
     s_row[j] = p.scale * dot;
   }
@@ -108,7 +117,7 @@ void one_row(const Problem& p, int64_t flat_row, double* o_row, double* lse_out,
     if (s_row[j] == neg_inf) continue;
     const double e = std::exp(s_row[j] - m);
     l += e;
-    for (int64_t d = 0; d < p.D; ++d) o_row[d] += e * bf16_to_double(vbh[j * p.D + d]);
+    for (int64_t d = 0; d < p.D; ++d) o_row[d] += e * v_at(p, vbh + j * p.D + d);
   }
   for (int64_t d = 0; d < p.D; ++d) o_row[d] /= l;
   *lse_out = m + std::log(l);
@@ -125,27 +134,20 @@ uint64_t attn_ref_score_buffer_bytes(int64_t B, int64_t H, int64_t s, int64_t e)
          static_cast<uint64_t>(s) * static_cast<uint64_t>(e);
 }
 
-// Reference attention forward in float64.
-//   q: bf16 bits [B][H][S_q][D]; k, v: bf16 bits [B][H][S_kv][D] (host memory)
-//   kv_valid_len: host int32[B] or null (= S_kv for every batch)
-//   rows: flat query-row ids (b*H + h)*S_q + i, or null for all B*H*S_q rows
-//   o: n_rows x D doubles; lse: n_rows doubles (natural log)
-//   threads <= 0 uses every hardware thread.
-// Returns 0 on success, 1 on invalid arguments.
-int attn_ref_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t B, int64_t H,
-                 int64_t S_q, int64_t S_kv, int64_t D, double scale, int causal,
-                 const int32_t* kv_valid_len, const int64_t* rows, int64_t n_rows, double* o,
-                 double* lse, int threads) {
-  if (B < 1 || H < 1 || S_q < 0 || S_kv < 0 || D < 1 || n_rows < 0) return 1;
-  if (n_rows > 0 && (q == nullptr || o == nullptr || lse == nullptr)) return 1;
-  if (S_kv > 0 && (k == nullptr || v == nullptr)) return 1;
+}  // extern "C"
+
+namespace {
+
+int run_rows(const Problem& p, const int64_t* rows, int64_t n_rows, double* o, double* lse, int threads) {
+  const int64_t B = p.B, H = p.H, S_q = p.S_q, D = p.D;
+  if (B < 1 || H < 1 || S_q < 0 || p.S_kv < 0 || D < 1 || n_rows < 0) return 1;
+  if (n_rows > 0 && (o == nullptr || lse == nullptr)) return 1;
   if (rows == nullptr && n_rows != B * H * S_q) return 1;
   const int64_t total = B * H * S_q;
   if (rows != nullptr) {
     for (int64_t r = 0; r < n_rows; ++r)
       if (rows[r] < 0 || rows[r] >= total) return 1;
   }
-  const Problem p{q, k, v, B, H, S_q, S_kv, D, scale, causal, kv_valid_len};
 
   int nt = threads > 0 ? threads : static_cast<int>(std::thread::hardware_concurrency());
   nt = std::max(1, std::min<int>(nt, static_cast<int>(std::max<int64_t>(n_rows, 1))));
@@ -166,6 +168,38 @@ int attn_ref_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_
     for (auto& th : pool) th.join();
   }
   return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Reference attention forward in float64.
+//   q: bf16 bits [B][H][S_q][D]; k, v: bf16 bits [B][H][S_kv][D] (host memory)
+//   kv_valid_len: host int32[B] or null (= S_kv for every batch)
+//   rows: flat query-row ids (b*H + h)*S_q + i, or null for all B*H*S_q rows
+//   o: n_rows x D doubles; lse: n_rows doubles (natural log)
+//   threads <= 0 uses every hardware thread.
+// Returns 0 on success, 1 on invalid arguments.
+int attn_ref_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t B, int64_t H,
+                 int64_t S_q, int64_t S_kv, int64_t D, double scale, int causal,
+                 const int32_t* kv_valid_len, const int64_t* rows, int64_t n_rows, double* o,
+                 double* lse, int threads) {
+  if (n_rows > 0 && q == nullptr) return 1;
+  if (S_kv > 0 && (k == nullptr || v == nullptr)) return 1;
+  const Problem p{q, k, v, nullptr, nullptr, nullptr, B, H, S_q, S_kv, D, scale, causal, kv_valid_len};
+  return run_rows(p, rows, n_rows, o, lse, threads);
+}
+
+// The same computation on float64 inputs (same layouts), for finite differences.
+int attn_ref_f64_dbl(const double* q, const double* k, const double* v, int64_t B, int64_t H,
+                     int64_t S_q, int64_t S_kv, int64_t D, double scale, int causal,
+                     const int32_t* kv_valid_len, const int64_t* rows, int64_t n_rows, double* o,
+                     double* lse, int threads) {
+  if (n_rows > 0 && q == nullptr) return 1;
+  if (S_kv > 0 && (k == nullptr || v == nullptr)) return 1;
+  const Problem p{nullptr, nullptr, nullptr, q, k, v, B, H, S_q, S_kv, D, scale, causal, kv_valid_len};
+  return run_rows(p, rows, n_rows, o, lse, threads);
 }
 
 // Threads attn_ref_f64 would use for threads <= 0.

@@ -21,15 +21,17 @@ MUTANTS = {
     "causal_excludes_diagonal": ("if (p.causal && j > i) return false;",
                                  "if (p.causal && j >= i) return false;"),
     "padding_off_by_one": ("if (j >= valid) return false;", "if (j > valid) return false;"),
-    "q_dot_v_instead_of_k": ("bf16_to_double(kbh[j * p.D + d])", "bf16_to_double(vbh[j * p.D + d])"),
+    "q_dot_v_instead_of_k": ("q_at(p, qi + d) * k_at(p, kbh + j * p.D + d)",
+                             "q_at(p, qi + d) * v_at(p, vbh + j * p.D + d)"),
     "no_normalisation": ("o_row[d] /= l;", "o_row[d] /= 1.0;"),
     "lse_without_max": ("*lse_out = m + std::log(l);", "*lse_out = std::log(l);"),
     "lse_base2": ("*lse_out = m + std::log(l);", "*lse_out = m + std::log2(l);"),
     "valid_len_of_batch0": ("std::max<int64_t>(p.kv_valid_len[b], 0)",
                             "std::max<int64_t>(p.kv_valid_len[0], 0)"),
-    "k_head_index_dropped": ("p.k + (b * p.H + h) * p.S_kv * p.D", "p.k + (b * p.H + 0) * p.S_kv * p.D"),
-    "v_row_index_shifted": ("e * bf16_to_double(vbh[j * p.D + d])",
-                            "e * bf16_to_double(vbh[((j + 1) % p.S_kv) * p.D + d])"),
+    "k_head_index_dropped": ("const int64_t kbh = (b * p.H + h) * p.S_kv * p.D;",
+                             "const int64_t kbh = (b * p.H + 0) * p.S_kv * p.D;"),
+    "v_row_index_shifted": ("e * v_at(p, vbh + j * p.D + d)",
+                            "e * v_at(p, vbh + ((j + 1) % p.S_kv) * p.D + d)"),
 }
 
 
