@@ -98,6 +98,34 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
                            const int32_t* kv_valid_len, void* stream);
 
 /*
+ * attn_bwd -- gradients of attn_fwd's O for a loss with gradient d_o:
+ *   P = exp(scale*S - LSE),  dV = P^T dO,  dP = dO V^T,
+ *   dS = P * (dP - rowsum(dO * O)),  dQ = scale dS K,  dK = scale dS^T Q,
+ * with the same masking as attn_fwd (masked pairs have P = 0).  The "Attention
+ * memory" page ("What this memory is") notes that training keeps the s x s
+ * scores for this pass unless a fused kernel intervenes; this one recomputes
+ * every score tile on chip from Q, K and the forward pass's LSE instead.
+ *
+ *   q, k, v, o, lse   the inputs and outputs of attn_fwd for the same
+ *                     arguments (o bf16 [B][H][S_q][D], lse fp32 [B][H][S_q]).
+ *   d_o               device bf16 [B][H][S_q][D], 16-byte aligned.
+ *   dq, dk, dv        device bf16, shaped like q, k, v, 16-byte aligned; written.
+ *   workspace         caller-owned device buffer, 16-byte aligned, at least
+ *                     attn_bwd_workspace_bytes(B, H, S_q, D) bytes (fp32
+ *                     per-row statistics and the dQ accumulator); overwritten.
+ * D is 64 or 128.  Asynchronous (three kernel launches on `stream`); argument
+ * errors are reported before anything is launched.  Key rows that no query
+ * may see get dK = dV = 0.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* d_o, void* dq, void* dk, void* dv, int B, int H, int S_q, int S_kv,
+                       int D, float scale, int causal, const int32_t* kv_valid_len, void* workspace,
+                       uint64_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_bwd needs (0 for invalid arguments). */
+uint64_t attn_bwd_workspace_bytes(int B, int H, int S_q, int D);
+
+/*
  * attn_fwd_splitkv -- the same result as attn_fwd, with the keys of every
  * query tile split into `n_splits` contiguous chunks of whole 128-key tiles
  * that are computed independently (more parallel work when B*H*ceil(S_q/256)

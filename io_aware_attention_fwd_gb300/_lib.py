@@ -20,7 +20,7 @@ ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_DEVICE = 6
 
 # every extern "C" function include/attn_fwd.h declares
-EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
+EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
             "attn_fwd_splitkv_suggest", "attn_merge", "attn_fwd_splitkv_static", "attn_status_str", "attn_fwd_debug_status",
             "attn_watchdog_selftest", "attn_fwd_abi_version")
 
@@ -57,6 +57,10 @@ def load() -> ctypes.CDLL:
             lib.attn_fwd_splitkv_suggest.restype = i
             lib.attn_fwd_splitkv_suggest.argtypes = [i, i, i, i, i, i]
             f = ctypes.c_float
+            lib.attn_bwd.restype = i
+            lib.attn_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, p, p, u64, p]
+            lib.attn_bwd_workspace_bytes.restype = u64
+            lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
             lib.attn_fwd_fp8.restype = i
             lib.attn_fwd_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, f, f, f, f, i, p, p]
             lib.attn_fwd_splitkv_static.restype = i
@@ -120,6 +124,22 @@ def attn_fwd_fp8(q, k, v, o, lse, B: int, H: int, S_q: int, S_kv: int, D: int, s
                              _addr(kv_valid_len), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_fp8")
+
+
+def attn_bwd(q, k, v, o, lse, d_o, dq, dk, dv, B: int, H: int, S_q: int, S_kv: int, D: int,
+             scale: float, causal: bool, kv_valid_len, workspace, workspace_bytes: int,
+             stream=None) -> None:
+    """Enqueue the backward pass (see include/attn_fwd.h)."""
+    st = load().attn_bwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(d_o), _addr(dq),
+                         _addr(dk), _addr(dv), int(B), int(H), int(S_q), int(S_kv), int(D),
+                         float(scale), int(bool(causal)), _addr(kv_valid_len), _addr(workspace),
+                         int(workspace_bytes), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, S_q: int, D: int) -> int:
+    return int(load().attn_bwd_workspace_bytes(int(B), int(H), int(S_q), int(D)))
 
 
 def attn_fwd_splitkv(q, k, v, o, lse, B: int, H: int, S_q: int, S_kv: int, D: int, scale: float,

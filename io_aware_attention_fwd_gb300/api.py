@@ -51,3 +51,29 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
     else:
         _lib.attn_fwd(q, k, v, out, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len, stream)
     return out, lse
+
+
+def attention_backward(q, k, v, o, lse, d_o, scale: float | None = None, causal: bool = False,
+                       kv_valid_len=None, stream=None):
+    """dQ, dK, dV (bf16) for the forward pass that produced (o, lse) from q, k, v.
+
+    All tensors are contiguous CUDA tensors as attention_forward uses them; d_o
+    is bf16 [B,H,S_q,D].  The fp32 workspace comes from torch's allocator.
+    """
+    import torch
+
+    B, H, S_q, D = q.shape
+    S_kv = k.shape[2]
+    for t in (q, k, v, o, d_o):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, d_o must be contiguous bf16 CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = _lib.attn_bwd_workspace_bytes(B, H, S_q, D)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    _lib.attn_bwd(q, k, v, o, lse, d_o, dq, dk, dv, B, H, S_q, S_kv, D, scale, causal, kv_valid_len,
+                  ws, nbytes, stream)
+    return dq, dk, dv

@@ -1,0 +1,522 @@
+// Backward pass of the fused attention, for GB300 (sm_103a).  Included by
+// attn_fwd.cu, whose PTX wrappers (TMA, mbarrier, tcgen05) it uses.
+//
+// Gradients of O = softmax(scale * Q K^T + mask) V for a loss with gradient dO:
+//   P   = exp(scale * S - LSE)          (recomputed; LSE from the forward pass)
+//   dV  = P^T dO
+//   dP  = dO V^T
+//   dS  = P * (dP - Delta),  Delta_i = sum_d dO_id O_id  (= sum_j P_ij dP_ij)
+//   dQ  = scale * dS K,      dK = scale * dS^T Q
+// The training frameworks the "Attention memory" page mentions ("What this
+// memory is") keep the s x s scores for this pass unless a fused kernel
+// intervenes; here every s x s tile is recomputed on chip from Q, K and the
+// per-row LSE, so the backward pass also never holds S or P in HBM.
+//
+// Kernels:
+//   attn_bwd_prep     Delta and LSE*log2(e) per query row (padded to whole
+//                     128-row tiles, +inf on padding so P = 0 there), and a
+//                     zeroed fp32 dQ accumulator.
+//   attn_bwd_sm103a   one CTA per (batch*head, 128-key tile j) walks the query
+//                     tiles that see those keys:
+//       warp 0        TMA: K_j and V_j once; Q_i into a 2-slot ring and dO_i
+//                     into a 1-slot ring.
+//       warp 1        tcgen05.mma, warp-wide with one elected issuing lane:
+//                       S^T  = K_j Q_i^T            (SS, into TMEM cols [0,128))
+//                       dP^T = V_j dO_i^T           (SS, cols [128,256))
+//                       dV  += P^T dO_i             (TS: P^T from TMEM)
+//                       dK  += dS^T Q_i             (TS: dS^T from TMEM)
+//                       dQ_i = dS K_j               (SS: dS from shared memory,
+//                                                    into cols [128,128+D))
+//       warps 4-7     one key row per thread: P^T and dS^T for the tile
+//                     (bf16, back into TMEM and, for dS, into shared memory);
+//                     at the end dK and dV out of TMEM into bf16 rows.
+//       warps 8-11    one query row per thread: dQ_i out of TMEM, reduce-added
+//                     into the fp32 accumulator.
+//   attn_bwd_dq_convert  dQ = bf16(scale * accumulator).
+// TMEM: S^T | dP^T (then dQ_i) | dV | dK, 512 columns at D = 128.
+
+// (Included inside attn_fwd.cu's anonymous namespace.)
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kPanels = D / 64;
+  static constexpr int kTileBytes = 128 * D * 2;  // one [128 x D] bf16 tile
+  static constexpr int kQSlots = 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQOff = 2 * kTileBytes;
+  static constexpr int kDOOff = kQOff + kQSlots * kTileBytes;
+  static constexpr int kDSOff = kDOOff + kTileBytes;           // dS^T [128 keys][128 queries] bf16
+  static constexpr int kDSBytes = 128 * 128 * 2;
+  static constexpr int kStatOff = kDSOff + kDSBytes;           // [2 tiles][lse2 | delta][128] fp32
+  static constexpr int kBarOff = kStatOff + 2 * 2 * 128 * 4;
+  // kv_full | q_full[2] | q_empty[2] | do_full | do_empty | s_full | dp_full | p_ready |
+  // ds_ready | dq_full | dq_free | dsm_free | done | drain | stat[2]
+  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 + 9 + 2;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;      // [0] tmem base, [1] abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+struct BwdParams {
+  float* dq_acc;            // fp32 [BH][S_q][D], zeroed by attn_bwd_prep
+  const float* lse2;        // [BH][S_pad]: LSE * log2(e); +inf for padding and key-less rows
+  const float* delta;       // [BH][S_pad]
+  uint16_t* dk;             // bf16 [BH][S_kv][D]
+  uint16_t* dv;             // bf16 [BH][S_kv][D]
+  const int32_t* kv_valid;
+  int S_q, S_kv, S_pad, H, BH, n_kv_tiles, n_q_tiles;
+  float scale_log2;         // scale * log2(e)
+  float scale;
+  int causal;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct BwdSmem {
+  uint32_t base;
+  __device__ uint32_t k() const { return base + BwdCfg<D>::kKOff; }
+  __device__ uint32_t v() const { return base + BwdCfg<D>::kVOff; }
+  __device__ uint32_t q(int s) const { return base + BwdCfg<D>::kQOff + s * BwdCfg<D>::kTileBytes; }
+  __device__ uint32_t d_o() const { return base + BwdCfg<D>::kDOOff; }
+  __device__ uint32_t ds() const { return base + BwdCfg<D>::kDSOff; }
+  __device__ uint32_t bar(int i) const { return base + BwdCfg<D>::kBarOff + 8 * i; }
+  __device__ uint32_t kv_full() const { return bar(0); }
+  __device__ uint32_t q_full(int s) const { return bar(1 + s); }
+  __device__ uint32_t q_empty(int s) const { return bar(3 + s); }
+  __device__ uint32_t do_full() const { return bar(5); }
+  __device__ uint32_t do_empty() const { return bar(6); }
+  __device__ uint32_t s_full() const { return bar(7); }
+  __device__ uint32_t dp_full() const { return bar(8); }
+  __device__ uint32_t p_ready() const { return bar(9); }
+  __device__ uint32_t ds_ready() const { return bar(10); }
+  __device__ uint32_t dq_full() const { return bar(11); }
+  __device__ uint32_t dq_free() const { return bar(12); }
+  __device__ uint32_t dsm_free() const { return bar(13); }
+  __device__ uint32_t done() const { return bar(14); }
+  __device__ uint32_t drain() const { return bar(15); }
+  __device__ uint32_t stat(int b) const { return bar(16 + b); }
+};
+
+// What one CTA covers: key tile j of head bh against query tiles
+// [i0, i0 + n).  Causal: only query tiles holding a query >= the first key.
+struct BwdWork {
+  int bh, k0, nk_pad, i0, n;
+};
+
+__device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
+  BwdWork w;
+  w.bh = static_cast<int>(blockIdx.x) / p.n_kv_tiles;
+  w.k0 = (static_cast<int>(blockIdx.x) % p.n_kv_tiles) * kBN;
+  int nk = p.S_kv;
+  if (p.kv_valid != nullptr) nk = min(max(__ldg(p.kv_valid + w.bh / p.H), 0), nk);
+  w.nk_pad = nk;
+  w.i0 = p.causal ? min(w.k0 / kBM, p.n_q_tiles) : 0;
+  w.n = (w.k0 < nk) ? p.n_q_tiles - w.i0 : 0;  // no valid key in the tile: gradients are zero
+  return w;
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4_b32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// TMA producer (one thread).
+template <int D>
+__device__ void bwd_load_role(const BwdSmem<D>& sm, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                              const CUtensorMap* tmV, const CUtensorMap* tmDO, const BwdWork& wk,
+                              const WaitCtx& w) {
+  using C = BwdCfg<D>;
+  tma_prefetch_desc(tmQ);
+  tma_prefetch_desc(tmK);
+  tma_prefetch_desc(tmV);
+  tma_prefetch_desc(tmDO);
+  mbar_expect_tx(sm.kv_full(), 2 * C::kTileBytes);
+  for (int pn = 0; pn < C::kPanels; ++pn) {
+    tma_load_3d(sm.k() + pn * kPanelBytes, tmK, sm.kv_full(), pn * 64, wk.k0, wk.bh);
+    tma_load_3d(sm.v() + pn * kPanelBytes, tmV, sm.kv_full(), pn * 64, wk.k0, wk.bh);
+  }
+  int nq = 0, ndo = 0;  // Q and dO tiles issued
+  for (int t = 0; t < wk.n; ++t) {
+    const int y = (wk.i0 + t) * kBM;
+    const int qs = t % C::kQSlots;
+    if (t >= C::kQSlots && !mbar_wait(sm.q_empty(qs), ((t / C::kQSlots) - 1) & 1, w)) break;
+    mbar_expect_tx(sm.q_full(qs), C::kTileBytes);
+    for (int pn = 0; pn < C::kPanels; ++pn) tma_load_3d(sm.q(qs) + pn * kPanelBytes, tmQ, sm.q_full(qs), pn * 64, y, wk.bh);
+    ++nq;
+    if (t > 0 && !mbar_wait(sm.do_empty(), (t - 1) & 1, w)) break;
+    mbar_expect_tx(sm.do_full(), C::kTileBytes);
+    for (int pn = 0; pn < C::kPanels; ++pn) tma_load_3d(sm.d_o() + pn * kPanelBytes, tmDO, sm.do_full(), pn * 64, y, wk.bh);
+    ++ndo;
+  }
+  // every issued copy lands before the CTA may exit (one shared deadline)
+  bool drained = mbar_wait_drain(sm.kv_full(), 0, w);
+  for (int u = (nq > C::kQSlots ? nq - C::kQSlots : 0); u < nq && drained; ++u)
+    drained = mbar_wait_drain(sm.q_full(u % C::kQSlots), (u / C::kQSlots) & 1, w);
+  if (drained && ndo > 0) mbar_wait_drain(sm.do_full(), (ndo - 1) & 1, w);
+}
+
+// MMA issuer: warp-wide control flow, one elected lane issues.
+template <int D>
+__device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork& wk, const WaitCtx& w) {
+  using C = BwdCfg<D>;
+  constexpr uint32_t idesc_s = make_idesc(kBM, kBN, false, false, false);  // [128 x 128], K-major A and B
+  constexpr uint32_t idesc_acc = make_idesc(kBM, D, false, true, false);   // TS: B MN-major
+  constexpr uint32_t idesc_dq = make_idesc(kBM, D, true, true, false);     // SS: A and B MN-major
+  const uint32_t leader = elect_one();
+  const uint64_t kd = sdesc_kmajor_sw128(sm.k());
+  const uint64_t vd = sdesc_kmajor_sw128(sm.v());
+  const uint64_t k_mn = sdesc_mnmajor_sw128(sm.k(), kPanelBytes);
+  const uint64_t ds_mn = sdesc_mnmajor_sw128(sm.ds(), kPanelBytes);
+  const uint64_t do_k = sdesc_kmajor_sw128(sm.d_o());
+  const uint64_t do_mn = sdesc_mnmajor_sw128(sm.d_o(), kPanelBytes);
+  const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDPCol, tDV = tmem + C::kDVCol, tDK = tmem + C::kDKCol;
+  bool ok = __all_sync(0xffffffffu, mbar_wait(sm.kv_full(), 0, w) && mbar_wait(sm.q_full(0), 0, w));
+  bool issued = false;
+  if (ok) {
+    tc_fence_after();
+    issue_qk<D, false>(leader, tS, kd, sdesc_kmajor_sw128(sm.q(0)), idesc_s);  // S^T_0 = K Q_0^T
+    tc_commit_if(leader, sm.s_full());
+    issued = true;
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.do_full(), 0, w));
+  }
+  if (ok) {
+    tc_fence_after();
+    issue_qk<D, false>(leader, tDP, vd, do_k, idesc_s);  // dP^T_0 = V dO_0^T
+    tc_commit_if(leader, sm.dp_full());
+  }
+  for (int t = 0; t < wk.n && ok; ++t) {
+    const int qs = t % C::kQSlots;
+    const uint64_t q_mn = sdesc_mnmajor_sw128(sm.q(qs), kPanelBytes);
+    // dV += P^T dO_t  (P^T read from TMEM before S^T_{t+1} overwrites it: in-order MMAs)
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.p_ready(), t & 1, w));
+    if (!ok) break;
+    tc_fence_after();
+    issue_pv<D, false>(leader, tDV, tS, do_mn, idesc_acc, t > 0);
+    tc_commit_if(leader, sm.do_empty());
+    if (t + 1 < wk.n) {  // S^T_{t+1}
+      const int qn = (t + 1) % C::kQSlots;
+      ok = __all_sync(0xffffffffu, mbar_wait(sm.q_full(qn), ((t + 1) / C::kQSlots) & 1, w));
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk<D, false>(leader, tS, kd, sdesc_kmajor_sw128(sm.q(qn)), idesc_s);
+      tc_commit_if(leader, sm.s_full());
+    }
+    // dK += dS^T Q_t (dS^T from TMEM), then dQ_t = dS K into the dP^T columns
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.ds_ready(), t & 1, w));
+    if (!ok) break;
+    tc_fence_after();
+    issue_pv<D, false>(leader, tDK, tDP, q_mn, idesc_acc, t > 0);
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+      const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+      mma_ss_if<false>(leader, tDP, ds_mn + off, k_mn + off, idesc_dq, kk > 0 ? 1u : 0u);
+    }
+    tc_commit_if(leader, sm.dq_full());
+    tc_commit_if(leader, sm.dsm_free());
+    tc_commit_if(leader, sm.q_empty(qs));
+    if (t + 1 < wk.n) {  // dP^T_{t+1}, once dQ_t has been read out of its columns
+      ok = __all_sync(0xffffffffu, mbar_wait(sm.do_full(), (t + 1) & 1, w) && mbar_wait(sm.dq_free(), t & 1, w));
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk<D, false>(leader, tDP, vd, do_k, idesc_s);
+      tc_commit_if(leader, sm.dp_full());
+    }
+  }
+  if (issued) {
+    tc_commit_if(leader, sm.done());
+    tc_commit_if(leader, sm.drain());
+    __all_sync(0xffffffffu, mbar_wait_drain(sm.drain(), 0, w));
+  }
+}
+
+// Key rows (128 threads): P^T and dS^T per query tile; dK, dV at the end.
+template <int D>
+__device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem, const BwdParams& p,
+                             const BwdWork& wk, const WaitCtx& w) {
+  using C = BwdCfg<D>;
+  const int r = static_cast<int>(threadIdx.x) - 128;  // key row == TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_off + C::kSCol;
+  const uint32_t tDP = tmem + lane_off + C::kDPCol;
+  const int key = wk.k0 + r;
+  const bool key_ok = key < wk.nk_pad;
+  const float c = p.scale_log2;
+  float* stats = reinterpret_cast<float*>(smem + C::kStatOff);
+  bool ok = true;
+  for (int t = 0; t < wk.n && ok; ++t) {
+    const int q0 = (wk.i0 + t) * kBM;
+    // this tile's lse2 and delta, one value per thread into a double buffer;
+    // buffer t&1 is rewritten two tiles later, after every thread has passed
+    // the next tile's barrier (so it has finished reading this one)
+    float* st = stats + (t & 1) * 256;  // [lse2 | delta] of this tile
+    const int64_t srow = static_cast<int64_t>(wk.bh) * p.S_pad + q0 + r;
+    st[r] = __ldg(p.lse2 + srow);
+    st[128 + r] = __ldg(p.delta + srow);
+    mbar_arrive(sm.stat(t & 1));
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.stat(t & 1), (t >> 1) & 1, w));
+    if (!ok) break;
+
+    // P^T row: p_c = 2^(c*s_c - lse2_c) for the allowed (key, query) pairs
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.s_full(), t & 1, w));
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t sr[128];
+    tmem_ld32(tS + 0, sr + 0);
+    tmem_ld32(tS + 32, sr + 32);
+    tmem_ld32(tS + 64, sr + 64);
+    tmem_ld32(tS + 96, sr + 96);
+    tmem_wait_ld();
+    const bool diag = p.causal && q0 < wk.k0 + kBN;  // some query of the tile precedes some key
+    uint32_t pk[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      float pv[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = 2 * i + e;
+        const float lse2 = st[col];
+        bool allowed = key_ok;
+        if (diag) allowed = allowed && (q0 + col >= key);
+        pv[e] = allowed ? ex2_approx(fmaf(__uint_as_float(sr[col]), c, -lse2)) : 0.f;
+      }
+      pk[i] = pack_bf16x2(pv[0], pv[1]);
+    }
+    tmem_st32(tS + 0, pk + 0);
+    tmem_st32(tS + 32, pk + 32);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(sm.p_ready());
+
+    // dS^T row: p * (dP^T - delta), to TMEM (for dK) and shared memory (for dQ)
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.dp_full(), t & 1, w));
+    if (ok && t > 0) ok = __all_sync(0xffffffffu, mbar_wait(sm.dsm_free(), (t - 1) & 1, w));
+    if (!ok) break;
+    tc_fence_after();
+#pragma unroll
+    for (int cc = 0; cc < 128; cc += 32) {
+      uint32_t dpr[32];
+      tmem_ld32(tDP + cc, dpr);
+      tmem_wait_ld();
+      uint32_t dsw[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t pw = pk[(cc >> 1) + i];
+        const float p0 = __uint_as_float(pw << 16), p1 = __uint_as_float(pw & 0xFFFF0000u);
+        const float d0 = p0 * (__uint_as_float(dpr[2 * i]) - st[128 + cc + 2 * i]);
+        const float d1 = p1 * (__uint_as_float(dpr[2 * i + 1]) - st[128 + cc + 2 * i + 1]);
+        dsw[i] = pack_bf16x2(d0, d1);
+      }
+      tmem_st16(tDP + (cc >> 1), dsw);
+      // shared memory: row r of the [key][query] tile, 128-byte swizzled panels of 64 queries
+      const uint32_t row = sm.ds() + static_cast<uint32_t>((cc >> 6) * kPanelBytes + r * 128);
+      const int chunk0 = (cc & 63) >> 3;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        st_shared_v4_b32(row + static_cast<uint32_t>(((chunk0 + u) ^ (r & 7)) << 4), dsw[4 * u], dsw[4 * u + 1],
+                         dsw[4 * u + 2], dsw[4 * u + 3]);
+    }
+    tmem_wait_st();
+    fence_async_smem();
+    tc_fence_before();
+    mbar_arrive(sm.ds_ready());
+  }
+
+  // dK and dV rows out of TMEM (zero when the CTA had no work)
+  bool have = ok && wk.n > 0;
+  if (have) have = __all_sync(0xffffffffu, mbar_wait(sm.done(), 0, w));
+  if (have) tc_fence_after();
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (times scale)
+    const uint32_t src = tmem + lane_off + (which ? C::kDKCol : C::kDVCol);
+    uint16_t* dst = (which ? p.dk : p.dv) + (static_cast<int64_t>(wk.bh) * p.S_kv + key) * D;
+    const float f = which ? p.scale : 1.f;
+#pragma unroll 1
+    for (int cc = 0; cc < D; cc += 32) {
+      uint32_t a[32];
+      if (have) {
+        tmem_ld32(src + cc, a);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] = 0u;
+      }
+      if (key < p.S_kv) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            wv[e] = pack_bf16x2(__uint_as_float(a[8 * q + 2 * e]) * f, __uint_as_float(a[8 * q + 2 * e + 1]) * f);
+          st_global_v4(dst + cc + 8 * q, wv[0], wv[1], wv[2], wv[3]);
+        }
+      }
+    }
+  }
+}
+
+// Query rows (128 threads): dQ_i out of TMEM, reduce-added into the fp32 accumulator.
+template <int D>
+__device__ void bwd_dq_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdParams& p, const BwdWork& wk,
+                            const WaitCtx& w) {
+  using C = BwdCfg<D>;
+  const int r = static_cast<int>(threadIdx.x) - 256;  // query row in the tile == TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const uint32_t tQ = tmem + lane_off + C::kDPCol;
+  for (int t = 0; t < wk.n; ++t) {
+    if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), t & 1, w))) break;
+    tc_fence_after();
+    const int q = (wk.i0 + t) * kBM + r;
+    float* dst = p.dq_acc + (static_cast<int64_t>(wk.bh) * p.S_q + q) * D;
+#pragma unroll 1
+    for (int cc = 0; cc < D; cc += 32) {
+      uint32_t a[32];
+      tmem_ld32(tQ + cc, a);
+      tmem_wait_ld();
+      if (q < p.S_q) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          red_add_v4(dst + cc + e, __uint_as_float(a[e]), __uint_as_float(a[e + 1]), __uint_as_float(a[e + 2]),
+                     __uint_as_float(a[e + 3]));
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(sm.dq_free());
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const BwdSmem<D> sm{base};
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const BwdWork wk = bwd_work(p);
+
+  if (threadIdx.x == 0) {
+    mbar_init(sm.kv_full(), 1);
+    for (int s = 0; s < C::kQSlots; ++s) {
+      mbar_init(sm.q_full(s), 1);
+      mbar_init(sm.q_empty(s), 1);
+    }
+    mbar_init(sm.do_full(), 1);
+    mbar_init(sm.do_empty(), 1);
+    mbar_init(sm.s_full(), 1);
+    mbar_init(sm.dp_full(), 1);
+    mbar_init(sm.p_ready(), kBM);
+    mbar_init(sm.ds_ready(), kBM);
+    mbar_init(sm.dq_full(), 1);
+    mbar_init(sm.dq_free(), kBM);
+    mbar_init(sm.dsm_free(), 1);
+    mbar_init(sm.done(), 1);
+    mbar_init(sm.drain(), 1);
+    mbar_init(sm.stat(0), kBM);
+    mbar_init(sm.stat(1), kBM);
+    misc[1] = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(base + C::kMiscOff, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const WaitCtx w{p.timeout_ns, misc + 1};
+
+  if (warp == 0) {
+    if (lane == 0 && wk.n > 0) bwd_load_role<D>(sm, &tmQ, &tmK, &tmV, &tmDO, wk, w);
+  } else if (warp == 1) {
+    if (wk.n > 0) bwd_mma_role<D>(sm, tmem, wk, w);
+  } else if (warp >= 4 && warp < 8) {
+    bwd_row_role<D>(sm, smem, tmem, p, wk, w);
+  } else if (warp >= 8) {
+    bwd_dq_role<D>(sm, tmem, p, wk, w);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Delta_i = sum_d dO_id O_id and lse2_i = LSE_i log2(e) per query row, padded
+// to S_pad rows (+inf / 0 on padding and for rows without keys, so P = 0
+// there); zeroes the fp32 dQ accumulator.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_prep(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o,
+                                                     const float* __restrict__ lse, float* __restrict__ lse2,
+                                                     float* __restrict__ delta, float* __restrict__ dq_acc, int S_q,
+                                                     int S_pad, int64_t BH) {
+  constexpr int kPer = D / 32;
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t step = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = first; row < BH * S_pad; row += step) {
+    const int64_t bh = row / S_pad;
+    const int q = static_cast<int>(row % S_pad);
+    float acc = 0.f, l2 = INFINITY;
+    if (q < S_q) {
+      const int64_t e0 = (bh * S_q + q) * D + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        const float a = __uint_as_float(static_cast<uint32_t>(__ldg(o + e0 + e)) << 16);
+        const float b = __uint_as_float(static_cast<uint32_t>(__ldg(d_o + e0 + e)) << 16);
+        acc = fmaf(a, b, acc);
+        dq_acc[e0 + e] = 0.f;
+      }
+      const float l = __ldg(lse + bh * S_q + q);
+      l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      lse2[row] = l2;
+      delta[row] = q < S_q ? acc : 0.f;
+    }
+  }
+}
+
+// dQ = bf16(scale * accumulator), four elements per thread step.
+__global__ void __launch_bounds__(256) attn_bwd_dq_convert(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq,
+                                                           int64_t n4, float scale) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(dq_acc) + i);
+    uint2 out;
+    out.x = pack_bf16x2(a.x * scale, a.y * scale);
+    out.y = pack_bf16x2(a.z * scale, a.w * scale);
+    reinterpret_cast<uint2*>(dq)[i] = out;
+  }
+}
+

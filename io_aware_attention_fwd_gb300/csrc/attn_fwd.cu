@@ -995,6 +995,9 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
   }
 }
 
+// The backward pass (same anonymous namespace, same PTX wrappers).
+#include "attn_bwd.cuh"
+
 // Waits on a barrier nothing completes; the bounded wait must give up.
 __global__ void attn_watchdog_kernel(unsigned long long timeout_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -1072,7 +1075,11 @@ attn_status_t prepare_device(int dev) {
       cudaFuncSetAttribute(attn_fwd_sm103a<128, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128, false>::kSmemBytes) != cudaSuccess ||
       cudaFuncSetAttribute(attn_fwd_sm103a<128, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<128, true>::kSmemBytes) != cudaSuccess)
+                           Cfg<128, true>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_bwd_sm103a<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<64>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_bwd_sm103a<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<128>::kSmemBytes) != cudaSuccess)
     return ATTN_ERR_DEVICE;
   g_dev_sms[dev].store(std::max(1, sms), std::memory_order_relaxed);
   g_dev_state[dev].store(1, std::memory_order_release);
@@ -1151,6 +1158,58 @@ attn_status_t check_args(const void* q, const void* k, const void* v, const void
   const int64_t n_pairs = (static_cast<int64_t>(S_q) + kRowsPerUnit - 1) / kRowsPerUnit;
   if (BH * n_pairs > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
+}
+
+// Backward workspace: lse2 and delta [BH][S_pad] and the fp32 dQ accumulator
+// [BH][S_q][D], S_pad = S_q rounded up to whole 128-row tiles.
+uint64_t bwd_workspace_bytes(int64_t BH, int64_t S_q, int D) {
+  const int64_t S_pad = (S_q + kBM - 1) / kBM * kBM;
+  return static_cast<uint64_t>(2 * BH * S_pad + BH * S_q * D) * 4u;
+}
+
+template <int D>
+attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* d_o, void* dq, void* dk, void* dv, int B, int H, int S_q, int S_kv, float scale,
+                         int causal, const int32_t* kv_valid_len, void* workspace, int sms, cudaStream_t stream) {
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int S_pad = (S_q + kBM - 1) / kBM * kBM;
+  float* lse2 = static_cast<float*>(workspace);
+  float* delta = lse2 + BH * S_pad;
+  float* dq_acc = delta + BH * S_pad;
+  const int64_t prep_blocks = std::min<int64_t>((BH * S_pad + 7) / 8, static_cast<int64_t>(sms) * 16);
+  attn_bwd_prep<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_o), lse, lse2, delta, dq_acc, S_q, S_pad, BH);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_3d(&tq, q, D, S_q, BH) || !encode_3d(&tk, k, D, S_kv, BH) || !encode_3d(&tv, v, D, S_kv, BH) ||
+      !encode_3d(&tdo, d_o, D, S_q, BH))
+    return ATTN_ERR_LAUNCH;
+  BwdParams prm;
+  prm.dq_acc = dq_acc;
+  prm.lse2 = lse2;
+  prm.delta = delta;
+  prm.dk = static_cast<uint16_t*>(dk);
+  prm.dv = static_cast<uint16_t*>(dv);
+  prm.kv_valid = kv_valid_len;
+  prm.S_q = S_q;
+  prm.S_kv = S_kv;
+  prm.S_pad = S_pad;
+  prm.H = H;
+  prm.BH = static_cast<int>(BH);
+  prm.n_kv_tiles = (S_kv + kBN - 1) / kBN;
+  prm.n_q_tiles = S_pad / kBM;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  prm.scale = scale;
+  prm.causal = causal;
+  prm.timeout_ns = kDefaultTimeoutNs;
+  const int64_t grid = BH * prm.n_kv_tiles;
+  attn_bwd_sm103a<D><<<static_cast<unsigned>(grid), kThreads, BwdCfg<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, prm);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  const int64_t n4 = BH * S_q * D / 4;
+  const int64_t cv_blocks = std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(sms) * 16);
+  attn_bwd_dq_convert<<<static_cast<unsigned>(cv_blocks), 256, 0, stream>>>(dq_acc, static_cast<uint16_t*>(dq), n4,
+                                                                            scale);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 constexpr int kMaxSplits = 64;
@@ -1253,6 +1312,50 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   if (!get_encoder()) return ATTN_ERR_DEVICE;
   return launch<128, true>(q, k, v, o, lse, B, H, S_q, S_kv, static_cast<float>(s_all), causal, kv_valid_len,
                            g_dev_sms[dev].load(std::memory_order_relaxed), 1, nullptr, nullptr, st, v_descale);
+}
+
+uint64_t attn_bwd_workspace_bytes(int B, int H, int S_q, int D) {
+  if (B < 1 || H < 1 || S_q < 0 || (D != 64 && D != 128)) return 0;
+  return bwd_workspace_bytes(static_cast<int64_t>(B) * H, S_q, D);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* d_o,
+                       void* dq, void* dk, void* dv, int B, int H, int S_q, int S_kv, int D, float scale, int causal,
+                       const int32_t* kv_valid_len, void* workspace, uint64_t workspace_bytes, void* stream) {
+  const attn_status_t as = check_args(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len);
+  if (as != ATTN_OK) return as;
+  if (S_q > 0 && (d_o == nullptr || dq == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (S_kv > 0 && (dk == nullptr || dv == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(d_o, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16)) return ATTN_ERR_ALIGNMENT;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH * ((static_cast<int64_t>(S_kv) + kBN - 1) / kBN) > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const uint64_t need = bwd_workspace_bytes(BH, S_q, D);
+  if (S_q > 0 && S_kv > 0) {
+    if (workspace == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return ATTN_ERR_ALIGNMENT;
+    if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  }
+  if (S_q == 0 && S_kv == 0) return ATTN_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
+  const attn_status_t ps = prepare_device(dev);
+  if (ps != ATTN_OK) return ps;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (S_q == 0 || S_kv == 0) {  // no query or no key: every gradient is zero
+    const size_t kv_bytes = static_cast<size_t>(BH) * S_kv * D * 2, q_bytes = static_cast<size_t>(BH) * S_q * D * 2;
+    if ((kv_bytes && (cudaMemsetAsync(dk, 0, kv_bytes, st) != cudaSuccess ||
+                      cudaMemsetAsync(dv, 0, kv_bytes, st) != cudaSuccess)) ||
+        (q_bytes && cudaMemsetAsync(dq, 0, q_bytes, st) != cudaSuccess))
+      return ATTN_ERR_LAUNCH;
+    return ATTN_OK;
+  }
+  if (!get_encoder()) return ATTN_ERR_DEVICE;
+  const int sms = g_dev_sms[dev].load(std::memory_order_relaxed);
+  if (D == 64)
+    return launch_bwd<64>(q, k, v, o, lse, d_o, dq, dk, dv, B, H, S_q, S_kv, scale, causal, kv_valid_len, workspace,
+                          sms, st);
+  return launch_bwd<128>(q, k, v, o, lse, d_o, dq, dk, dv, B, H, S_q, S_kv, scale, causal, kv_valid_len, workspace,
+                         sms, st);
 }
 
 uint64_t attn_fwd_splitkv_workspace_bytes(int B, int H, int S_q, int D, int n_splits) {

@@ -162,3 +162,28 @@ def test_fp8_argument_checks(kw, expect):
                 scale=0.1, q_descale=1.0, k_descale=1.0, v_descale=1.0, causal=False)
     args.update(kw)
     assert attn.call_status(attn.attn_fwd_fp8, **args) == expect
+
+
+def test_bwd_workspace_size():
+    # lse2 and delta padded to whole 128-row tiles, plus the fp32 dQ accumulator
+    assert attn.attn_bwd_workspace_bytes(2, 3, 200, 64) == (2 * 6 * 256 + 6 * 200 * 64) * 4
+    assert attn.attn_bwd_workspace_bytes(1, 1, 10, 96) == 0
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d_o=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dq=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dk=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(workspace_bytes=100), attn.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=FAKE + 4), attn.ATTN_ERR_ALIGNMENT),
+    (dict(dv=FAKE + 2), attn.ATTN_ERR_ALIGNMENT),
+    (dict(D=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(scale=-1.0), attn.ATTN_ERR_INVALID_ARG),
+])
+def test_bwd_argument_checks(kw, expect):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, d_o=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, H=2,
+                S_q=128, S_kv=128, D=64, scale=0.125, causal=False, kv_valid_len=None, workspace=FAKE,
+                workspace_bytes=attn.attn_bwd_workspace_bytes(1, 2, 128, 64))
+    args.update(kw)
+    assert attn.call_status(attn.attn_bwd, **args) == expect
