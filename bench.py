@@ -70,6 +70,9 @@ WORKLOADS = {
                                          valid=(8192, 5000), dtype="e4m3", fp8_mult=16.0),
     "b1_h32_s32768_d128_fp8": dict(B=1, H=32, S=32768, D=128, modes=(True, False), seed=6,
                                    dtype="e4m3", fp8_mult=16.0),
+    # backward pass (dQ, dK, dV from Q, K, V, O, LSE, dO): 10 * D FLOPs per allowed pair
+    "b4_h16_s1024_d64_bwd": dict(B=4, H=16, S=1024, D=64, modes=(False, True), seed=2, pass_="bwd"),
+    "b1_h32_s8192_d128_bwd": dict(B=1, H=32, S=8192, D=128, modes=(True, False), seed=8, pass_="bwd"),
 }
 DEFAULT_WORKLOAD = "b4_h16_s1024_d64"
 
@@ -94,7 +97,10 @@ def s_kv(w):
 
 
 def alg_flops(w, causal):
-    return 4 * w["D"] * allowed_pairs(w["B"], w["H"], w["S"], s_kv(w), causal, w.get("valid"))
+    """4 D FLOPs per allowed (query, key) pair forward (QK^T and PV), 10 D
+    backward (QK^T, dO V^T, P^T dO, dS^T Q and dS K)."""
+    per = 10 if w.get("pass_") == "bwd" else 4
+    return per * w["D"] * allowed_pairs(w["B"], w["H"], w["S"], s_kv(w), causal, w.get("valid"))
 
 
 def alg_bytes(w, causal):
@@ -358,9 +364,25 @@ def main():
     ws_bytes = attn.attn_fwd_splitkv_workspace_bytes(B, H, S, D, splits) if splits > 1 else 0
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if splits > 1 else None
     kernels_per_call = 2 if splits > 1 else 1  # key-split calls add the merge kernel
+    bwd = w.get("pass_") == "bwd"
+    if bwd:  # inputs of the backward pass: dO plus the forward's O and LSE per mode
+        kernels_per_call = 3  # statistics, gradients, dQ conversion
+        d_o = si.normal_bf16_torch(w["seed"], 5, B * H * S * D, device=dev).view(B, H, S, D)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        fwd_out = {}
+        for causal in modes:
+            oo, ll = torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev)
+            attn.attn_fwd(q, k, v, oo, ll, B, H, S, S_kv, D, scale, causal, kvl, stream)
+            fwd_out[causal] = (oo, ll)
+        bws_bytes = attn.attn_bwd_workspace_bytes(B, H, S, D)
+        bws = torch.empty(bws_bytes, dtype=torch.uint8, device=dev)
 
     def launch(causal):
-        if fp8:
+        if bwd:
+            oo, ll = fwd_out[causal]
+            attn.attn_bwd(q, k, v, oo, ll, d_o, dq, dk, dv, B, H, S, S_kv, D, scale, causal, kvl, bws, bws_bytes,
+                          stream)
+        elif fp8:
             attn.attn_fwd_fp8(q, k, v, o, lse, B, H, S, S_kv, D, scale, descale, descale, descale, causal, kvl,
                               stream)
         elif splits > 1:
@@ -369,21 +391,22 @@ def main():
         else:
             attn.attn_fwd(q, k, v, o, lse, B, H, S, S_kv, D, scale, causal, kvl, stream)
 
-    # host buffers for the end-to-end leg
-    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
-    d2h = (ho.numel() * ho.element_size() + hl.numel() * hl.element_size()) * len(modes)
+    # host buffers for the end-to-end leg: the call's inputs go in, its outputs come out
+    ins = [q, k, v] + ([d_o] if bwd else [])
+    outs = [dq, dk, dv] if bwd else [o, lse]
+    h_ins = [x.cpu().pin_memory() for x in ins]
+    h_outs = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
+    hq, hk, hv = h_ins[:3]
+    h2d = sum(x.numel() * x.element_size() for x in h_ins)
+    d2h = sum(x.numel() * x.element_size() for x in h_outs) * len(modes)
 
     def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
+        for dst, src in zip(ins, h_ins):
+            dst.copy_(src, non_blocking=True)
         for causal in modes:
             launch(causal)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+            for dst, src in zip(h_outs, outs):
+                dst.copy_(src, non_blocking=True)
 
     for _ in range(args.warmup):
         for causal in modes:
@@ -467,7 +490,8 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
                      "alg_bytes_per_launch": sum(alg_bytes(w, c) for c in modes) / n_l,
-                     "kernel": (f"attn_fwd_sm103a<{D}, e4m3>" if fp8 else f"attn_fwd_sm103a<{D}>" if splits == 1 else
+                     "kernel": (f"attn_bwd_prep + attn_bwd_sm103a<{D}> + attn_bwd_dq_convert (one call)" if bwd else
+                                f"attn_fwd_sm103a<{D}, e4m3>" if fp8 else f"attn_fwd_sm103a<{D}>" if splits == 1 else
                                 f"attn_fwd_sm103a<{D}, split> + attn_merge_kernel<{D}> (one call, both timed)"),
                      "peak_source": peak_src},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

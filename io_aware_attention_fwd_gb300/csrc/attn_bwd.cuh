@@ -26,7 +26,10 @@
 //                       dV  += P^T dO_i             (TS: P^T from TMEM)
 //                       dK  += dS^T Q_i             (TS: dS^T from TMEM)
 //                       dQ_i = dS K_j               (SS: dS from shared memory,
-//                                                    into cols [128,128+D))
+//                                                    into cols [128,128+D));
+//                                                    at D = 128 as dQ_i^T = K_j^T dS^T
+//                                                    (lanes = head dim, coalesced
+//                                                    reduction per query)
 //       warps 4-7     one key row per thread: P^T and dS^T for the tile
 //                     (bf16, back into TMEM and, for dS, into shared memory);
 //                     at the end dK and dV out of TMEM into bf16 rows.
@@ -127,6 +130,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+__device__ __forceinline__ void red_add_f32(float* p, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
+}
+
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
@@ -181,6 +188,9 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
   constexpr uint32_t idesc_s = make_idesc(kBM, kBN, false, false, false);  // [128 x 128], K-major A and B
   constexpr uint32_t idesc_acc = make_idesc(kBM, D, false, true, false);   // TS: B MN-major
   constexpr uint32_t idesc_dq = make_idesc(kBM, D, true, true, false);     // SS: A and B MN-major
+  // D = 128: dQ_i^T = K_j^T dS^T instead (lanes = head dim), so each warp's
+  // reduction into the accumulator covers 32 consecutive floats of a row
+  constexpr bool kDqT = (D == 128);
   const uint32_t leader = elect_one();
   const uint64_t kd = sdesc_kmajor_sw128(sm.k());
   const uint64_t vd = sdesc_kmajor_sw128(sm.v());
@@ -228,7 +238,10 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk) {
       const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
-      mma_ss_if<false>(leader, tDP, ds_mn + off, k_mn + off, idesc_dq, kk > 0 ? 1u : 0u);
+      if (kDqT)
+        mma_ss_if<false>(leader, tDP, k_mn + off, ds_mn + off, idesc_dq, kk > 0 ? 1u : 0u);
+      else
+        mma_ss_if<false>(leader, tDP, ds_mn + off, k_mn + off, idesc_dq, kk > 0 ? 1u : 0u);
     }
     tc_commit_if(leader, sm.dq_full());
     tc_commit_if(leader, sm.dsm_free());
@@ -288,17 +301,19 @@ __device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem,
     const bool diag = p.causal && q0 < wk.k0 + kBN;  // some query of the tile precedes some key
     uint32_t pk[64];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      float pv[2];
+    for (int i = 0; i < 32; ++i) {  // four queries at a time
+      const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * i);
+      const float lse2[4] = {l4.x, l4.y, l4.z, l4.w};
+      float pv[4];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = 2 * i + e;
-        const float lse2 = st[col];
+      for (int e = 0; e < 4; ++e) {
+        const int col = 4 * i + e;
         bool allowed = key_ok;
         if (diag) allowed = allowed && (q0 + col >= key);
-        pv[e] = allowed ? ex2_approx(fmaf(__uint_as_float(sr[col]), c, -lse2)) : 0.f;
+        pv[e] = allowed ? ex2_approx(fmaf(__uint_as_float(sr[col]), c, -lse2[e])) : 0.f;
       }
-      pk[i] = pack_bf16x2(pv[0], pv[1]);
+      pk[2 * i] = pack_bf16x2(pv[0], pv[1]);
+      pk[2 * i + 1] = pack_bf16x2(pv[2], pv[3]);
     }
     tmem_st32(tS + 0, pk + 0);
     tmem_st32(tS + 32, pk + 32);
@@ -318,12 +333,17 @@ __device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem,
       tmem_wait_ld();
       uint32_t dsw[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t pw = pk[(cc >> 1) + i];
-        const float p0 = __uint_as_float(pw << 16), p1 = __uint_as_float(pw & 0xFFFF0000u);
-        const float d0 = p0 * (__uint_as_float(dpr[2 * i]) - st[128 + cc + 2 * i]);
-        const float d1 = p1 * (__uint_as_float(dpr[2 * i + 1]) - st[128 + cc + 2 * i + 1]);
-        dsw[i] = pack_bf16x2(d0, d1);
+      for (int i = 0; i < 8; ++i) {  // four queries at a time
+        const float4 d4 = *reinterpret_cast<const float4*>(st + 128 + cc + 4 * i);
+        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t pw = pk[(cc >> 1) + 2 * i + h];
+          const float p0 = __uint_as_float(pw << 16), p1 = __uint_as_float(pw & 0xFFFF0000u);
+          const float d0 = p0 * (__uint_as_float(dpr[4 * i + 2 * h]) - dl[2 * h]);
+          const float d1 = p1 * (__uint_as_float(dpr[4 * i + 2 * h + 1]) - dl[2 * h + 1]);
+          dsw[2 * i + h] = pack_bf16x2(d0, d1);
+        }
       }
       tmem_st16(tDP + (cc >> 1), dsw);
       // shared memory: row r of the [key][query] tile, 128-byte swizzled panels of 64 queries
@@ -384,22 +404,31 @@ __device__ void bwd_dq_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdParams
   for (int t = 0; t < wk.n; ++t) {
     if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), t & 1, w))) break;
     tc_fence_after();
-    const int q = (wk.i0 + t) * kBM + r;
-    float* dst = p.dq_acc + (static_cast<int64_t>(wk.bh) * p.S_q + q) * D;
-#pragma unroll 1
-    for (int cc = 0; cc < D; cc += 32) {
-      uint32_t a[32];
-      tmem_ld32(tQ + cc, a);
-      tmem_wait_ld();
+    const int q0 = (wk.i0 + t) * kBM;
+    // read the whole tile row first and release its TMEM columns (the next
+    // dP^T product waits for them), then reduce into the accumulator
+    uint32_t a[128];
+#pragma unroll
+    for (int cc = 0; cc < (D == 128 ? 128 : D); cc += 32) tmem_ld32(tQ + cc, a + cc);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(sm.dq_free());
+    if constexpr (D == 128) {  // lane r holds dQ^T[r][query]: one coalesced row segment per warp per query
+      float* col = p.dq_acc + (static_cast<int64_t>(wk.bh) * p.S_q + q0) * D + r;
+      const int nq = min(kBM, p.S_q - q0);
+#pragma unroll
+      for (int qq = 0; qq < 128; ++qq)
+        if (qq < nq) red_add_f32(col + static_cast<int64_t>(qq) * D, __uint_as_float(a[qq]));
+    } else {  // lane r holds dQ[query r][:]
+      const int q = q0 + r;
+      float* dst = p.dq_acc + (static_cast<int64_t>(wk.bh) * p.S_q + q) * D;
       if (q < p.S_q) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          red_add_v4(dst + cc + e, __uint_as_float(a[e]), __uint_as_float(a[e + 1]), __uint_as_float(a[e + 2]),
+        for (int e = 0; e < D; e += 4)
+          red_add_v4(dst + e, __uint_as_float(a[e]), __uint_as_float(a[e + 1]), __uint_as_float(a[e + 2]),
                      __uint_as_float(a[e + 3]));
       }
     }
-    tc_fence_before();
-    mbar_arrive(sm.dq_free());
   }
 }
 
