@@ -7,9 +7,12 @@ The attention arithmetic lives in ``attn_ref.cpp`` (plain float64 C++, one
 materialised score row per query, two-pass softmax).  This module compiles it
 with the host C++ compiler on first use (or from ``build()``) and calls it
 through ctypes; ``merge_f64`` (the log-sum-exp merge of results over disjoint
-key sets) is plain float64 numpy here.
+key sets) and ``attention_bwd_f64`` (the gradients, per head with P
+materialised) are plain float64 numpy here.
 
-Parity pins: ``tests/test_oracle_pins.py`` and ``tests/test_oracle_mutants.py``.
+Parity pins: ``tests/test_oracle_pins.py`` and ``tests/test_oracle_mutants.py``
+(forward, merge); ``tests/test_oracle_bwd_pins.py`` (gradients: finite
+differences of the C++ forward, torch float64 autograd, closed-form sums).
 """
 from __future__ import annotations
 

@@ -67,3 +67,29 @@ def test_backward_float_and_bf16_inputs_agree():
     b = oracle.attention_bwd_f64(*(si.bf16_bits_to_f32(x) for x in bits), 0.5, True)
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_sums_and_masked_keys(causal):
+    """Closed forms that hold for any inputs:
+    * Adding one vector to every key shifts each row's logits by a constant,
+      which the softmax ignores, so the key gradients of a head sum to zero.
+    * Each row of P sums to one, so the value gradients of a head sum to the
+      sum of dO over the rows that have at least one allowed key.
+    * A key past its batch's valid length gets exactly zero gradient, and a
+      batch with no valid key gets zero gradients everywhere."""
+    B, H, S_q, S_kv, D = 3, 2, 9, 11, 6
+    q = draws(63, (B, H, S_q, D), 1)
+    k = draws(63, (B, H, S_kv, D), 2)
+    v = draws(63, (B, H, S_kv, D), 3)
+    g = draws(63, (B, H, S_q, D), 5)
+    valid = [11, 4, 0]
+    dq, dk, dv = oracle.attention_bwd_f64(q, k, v, g, 0.7, causal, kv_valid_len=valid)
+    for b in range(B):
+        n = valid[b]
+        # with top-left causal alignment key 0 is allowed for every row
+        has_key = np.full(S_q, n > 0)
+        np.testing.assert_allclose(dk[b].sum(axis=1), 0.0, atol=1e-12)
+        np.testing.assert_allclose(dv[b].sum(axis=1), g[b][:, has_key].sum(axis=1), atol=1e-12)
+        assert np.all(dk[b, :, n:] == 0.0) and np.all(dv[b, :, n:] == 0.0)
+    assert np.all(dq[2] == 0.0)
