@@ -143,8 +143,11 @@ def load_peaks(dtype="bf16"):
 
 
 def kernel_source_hash():
-    src = ROOT / "io_aware_attention_fwd_gb300" / "csrc" / "attn_fwd.cu"
-    return hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    csrc = ROOT / "io_aware_attention_fwd_gb300" / "csrc"
+    h = hashlib.sha256()
+    for src in [csrc / "attn_fwd.cu", *sorted(csrc.glob("*.cuh"))]:
+        h.update(src.read_bytes())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload):

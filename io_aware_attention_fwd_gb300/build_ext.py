@@ -15,7 +15,7 @@ from pathlib import Path
 PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
 SOURCES = [PKG / "csrc" / "attn_fwd.cu"]
-HEADERS = [ROOT / "include" / "attn_fwd.h"]
+HEADERS = [ROOT / "include" / "attn_fwd.h", *sorted((PKG / "csrc").glob("*.cuh"))]
 BUILD_DIR = PKG / "_build"
 LIB_PATH = BUILD_DIR / "libattn_fwd.so"
 

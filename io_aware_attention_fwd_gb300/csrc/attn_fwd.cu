@@ -88,8 +88,8 @@ struct Cfg {
   static constexpr int kSlotOff = kQTiles * kTileBytes;
   static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
   // barriers: q_full | q_free[2] | full[kSlots] | empty[kSlots] | s_full[2] | p_full[2] |
-  //           o_done[2] | drain
-  static constexpr int kNumBars = 1 + kQTiles + 2 * kSlots + 3 * kQTiles + 1;
+  //           o_done[2] | drain | turn
+  static constexpr int kNumBars = 1 + kQTiles + 2 * kSlots + 3 * kQTiles + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] tmem base, [1] abort flag
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024 B alignment
   static constexpr int kOCol0 = kQTiles * kBN;             // first O column in TMEM
@@ -463,6 +463,7 @@ struct Smem {
   __device__ uint32_t bar_p(int t) const { return bar(1 + 2 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
   __device__ uint32_t bar_o(int t) const { return bar(1 + 3 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
   __device__ uint32_t bar_drain() const { return bar(1 + 4 * kQTiles + 2 * Cfg<D, kF8>::kSlots); }
+  __device__ uint32_t bar_turn() const { return bar(2 + 4 * kQTiles + 2 * Cfg<D, kF8>::kSlots); }
 };
 
 // One work unit: two 128-row query tiles of one (batch, head).
@@ -691,7 +692,8 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
   const float c = p.scale_log2;
   const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
   const int rounds = (p.n_units + G - 1) / G;
-  int cnt = 0;  // kv tiles this query tile has processed (S_full / O_done phases)
+  int cnt = 0;    // kv tiles this query tile has processed (S_full / O_done phases)
+  int sbase = 0;  // softmax steps of both query tiles in this CTA's earlier units
   bool ok = true;
   for (int rr = 0; rr < rounds && ok; ++rr) {
     const int u = unit_of(rr, cta, G);
@@ -702,11 +704,19 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
     int lim = un.mask_all ? 0 : un.nk_pad;  // keys j < lim are allowed for this row
     if (p.causal) lim = min(lim, row + 1);
     const int nkv = t ? un.nkv[1] : un.nkv[0];
+    const int n0 = un.nkv[0], n1 = un.nkv[1];
 
     float m_c = -INFINITY;  // running max, in scaled log2 units, as used for P
     float l = 0.f;          // running sum of P relative to m_c
     for (int j = 0; j < nkv; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_s(t), (cnt + j) & 1, w));
+      // The two softmax warpgroups take turns: the CTA's softmax steps are
+      // ordered per unit, per kv step, tile 0 before tile 1, and step n starts
+      // its exponentials only once step n - 1 has finished its own.  Each
+      // step then runs alone on the SM sub-partitions it shares with the
+      // other warpgroup while the tensor core serves the other query tile.
+      const int step = sbase + min(j, n0) + min(j, n1) + ((t == 1 && j < n0) ? 1 : 0);
+      ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_s(t), (cnt + j) & 1, w) &&
+                                       (step == 0 || mbar_wait(sm.bar_turn(), (step - 1) & 1, w)));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[kBN];
@@ -772,6 +782,7 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
       l = l * alpha + (sa + sb);
 #pragma unroll
       for (int cc = 0; cc < C::kPCols; cc += 32) tmem_st32(tS + cc, pk + cc);
+      mbar_arrive(sm.bar_turn());
       tmem_wait_st();
 
       // Lazy correction: O is rescaled only when some row's max grew by > 2^8.
@@ -809,6 +820,7 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
     bool have_o = ok;
     if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (cnt + nkv - 1) & 1, w));
     cnt += nkv;
+    sbase += n0 + n1;
     if (have_o) tc_fence_after();
     float inv_l = 0.f, lse = -INFINITY;
     if (l > 0.f) {
@@ -898,6 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sm.bar_o(t), 1);
     }
     mbar_init(sm.bar_drain(), 1);
+    mbar_init(sm.bar_turn(), kBM);
     misc[1] = 0u;
     fence_barrier_init();
   }
