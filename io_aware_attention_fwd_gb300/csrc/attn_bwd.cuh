@@ -146,6 +146,26 @@ __device__ __forceinline__ void st_shared_v4_b32(uint32_t addr, uint32_t a, uint
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// One key row of P^T for a query tile: p = 2^(c s - lse2) for its 128 query
+// columns, packed to bf16 pairs.  kMask: column col is allowed iff col >= first.
+template <bool kMask>
+__device__ __forceinline__ void bwd_p_row(const uint32_t* sr, const float* st, float c, int first, uint32_t* pk) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {  // four queries at a time
+    const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * i);
+    const float lse2[4] = {l4.x, l4.y, l4.z, l4.w};
+    float pv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float x = fmaf(__uint_as_float(sr[4 * i + e]), c, -lse2[e]);
+      if (kMask) x = (4 * i + e >= first) ? x : -INFINITY;
+      pv[e] = ex2_approx(x);
+    }
+    pk[2 * i] = pack_bf16x2(pv[0], pv[1]);
+    pk[2 * i + 1] = pack_bf16x2(pv[2], pv[3]);
+  }
+}
+
 // TMA producer (one thread).
 template <int D>
 __device__ void bwd_load_role(const BwdSmem<D>& sm, const CUtensorMap* tmQ, const CUtensorMap* tmK,
@@ -298,22 +318,17 @@ __device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem,
     tmem_ld32(tS + 64, sr + 64);
     tmem_ld32(tS + 96, sr + 96);
     tmem_wait_ld();
+    // Masking only on tiles that need it (the causal diagonal, or padded
+    // keys): query column col is allowed iff col >= first, and a masked score
+    // enters the exponential as -inf, so its P is exactly 0.  Both loops run
+    // without a branch per score.
     const bool diag = p.causal && q0 < wk.k0 + kBN;  // some query of the tile precedes some key
     uint32_t pk[64];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {  // four queries at a time
-      const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * i);
-      const float lse2[4] = {l4.x, l4.y, l4.z, l4.w};
-      float pv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = 4 * i + e;
-        bool allowed = key_ok;
-        if (diag) allowed = allowed && (q0 + col >= key);
-        pv[e] = allowed ? ex2_approx(fmaf(__uint_as_float(sr[col]), c, -lse2[e])) : 0.f;
-      }
-      pk[2 * i] = pack_bf16x2(pv[0], pv[1]);
-      pk[2 * i + 1] = pack_bf16x2(pv[2], pv[3]);
+    if (diag || wk.k0 + kBN > wk.nk_pad) {
+      const int first = !key_ok ? kBM : (diag ? key - q0 : 0);
+      bwd_p_row<true>(sr, st, c, first, pk);
+    } else {
+      bwd_p_row<false>(sr, st, c, 0, pk);
     }
     tmem_st32(tS + 0, pk + 0);
     tmem_st32(tS + 32, pk + 32);
