@@ -295,15 +295,25 @@ __device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem,
   const float c = p.scale_log2;
   float* stats = reinterpret_cast<float*>(smem + C::kStatOff);
   bool ok = true;
+  // lse2 and delta of query row r of the next tile, loaded one tile ahead
+  const int64_t srow0 = static_cast<int64_t>(wk.bh) * p.S_pad + wk.i0 * kBM + r;
+  float next_l2 = 0.f, next_dl = 0.f;
+  if (wk.n > 0) {
+    next_l2 = __ldg(p.lse2 + srow0);
+    next_dl = __ldg(p.delta + srow0);
+  }
   for (int t = 0; t < wk.n && ok; ++t) {
     const int q0 = (wk.i0 + t) * kBM;
     // this tile's lse2 and delta, one value per thread into a double buffer;
     // buffer t&1 is rewritten two tiles later, after every thread has passed
     // the next tile's barrier (so it has finished reading this one)
     float* st = stats + (t & 1) * 256;  // [lse2 | delta] of this tile
-    const int64_t srow = static_cast<int64_t>(wk.bh) * p.S_pad + q0 + r;
-    st[r] = __ldg(p.lse2 + srow);
-    st[128 + r] = __ldg(p.delta + srow);
+    st[r] = next_l2;
+    st[128 + r] = next_dl;
+    if (t + 1 < wk.n) {
+      next_l2 = __ldg(p.lse2 + srow0 + (t + 1) * kBM);
+      next_dl = __ldg(p.delta + srow0 + (t + 1) * kBM);
+    }
     mbar_arrive(sm.stat(t & 1));
     ok = __all_sync(0xffffffffu, mbar_wait(sm.stat(t & 1), (t >> 1) & 1, w));
     if (!ok) break;
