@@ -84,6 +84,7 @@ struct Cfg {
   static constexpr int kPvSteps = kBN / kKeysPerStep;
   static constexpr int kPCols = kBN * kEB / 4;        // TMEM columns of packed P
   static constexpr int kSlots = kF8 ? 12 : ((D == 128) ? 5 : 12);
+  static constexpr bool kTurn = !kF8 && D == 128;  // softmax warpgroups alternate
   static constexpr int kQOff = 0;
   static constexpr int kSlotOff = kQTiles * kTileBytes;
   static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
@@ -709,14 +710,16 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
     float m_c = -INFINITY;  // running max, in scaled log2 units, as used for P
     float l = 0.f;          // running sum of P relative to m_c
     for (int j = 0; j < nkv; ++j) {
-      // The two softmax warpgroups take turns: the CTA's softmax steps are
-      // ordered per unit, per kv step, tile 0 before tile 1, and step n starts
-      // its exponentials only once step n - 1 has finished its own.  Each
-      // step then runs alone on the SM sub-partitions it shares with the
-      // other warpgroup while the tensor core serves the other query tile.
+      // bf16 at D = 128: the two softmax warpgroups take turns.  The CTA's
+      // softmax steps are ordered per unit, per kv step, tile 0 before tile 1,
+      // and step n starts its exponentials only once step n - 1 has finished
+      // its own, so each runs alone on the SM sub-partitions it shares with
+      // the other warpgroup while the tensor core serves the other query
+      // tile.  (Measured: +2-3% there; at D = 64 and with e4m3 operands the
+      // MMAs are too short for the alternation to pay, and it costs ~8%.)
       const int step = sbase + min(j, n0) + min(j, n1) + ((t == 1 && j < n0) ? 1 : 0);
       ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_s(t), (cnt + j) & 1, w) &&
-                                       (step == 0 || mbar_wait(sm.bar_turn(), (step - 1) & 1, w)));
+                                       (!C::kTurn || step == 0 || mbar_wait(sm.bar_turn(), (step - 1) & 1, w)));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[kBN];
@@ -782,7 +785,7 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
       l = l * alpha + (sa + sb);
 #pragma unroll
       for (int cc = 0; cc < C::kPCols; cc += 32) tmem_st32(tS + cc, pk + cc);
-      mbar_arrive(sm.bar_turn());
+      if (C::kTurn) mbar_arrive(sm.bar_turn());
       tmem_wait_st();
 
       // Lazy correction: O is rescaled only when some row's max grew by > 2^8.
