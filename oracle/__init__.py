@@ -144,7 +144,7 @@ def _widen(x):
     return x.astype(np.float64)
 
 
-def attention_bwd_f64(q, k, v, d_o, scale: float, causal: bool, kv_valid_len=None):
+def attention_bwd_f64(q, k, v, d_o, scale: float, causal: bool, kv_valid_len=None, heads=None):
     """Gradients of the attention forward pass, in float64.
 
     q, d_o: [B,H,S_q,D]; k, v: [B,H,S_kv,D], as bf16 bit patterns (uint16) or
@@ -157,7 +157,10 @@ def attention_bwd_f64(q, k, v, d_o, scale: float, causal: bool, kv_valid_len=Non
     pass is the one the pages define ("Attention memory" page, "What this
     memory is"; masked keys as in the masked_fill sentences of the "PyTorch
     attention backends" story).  P is materialised per head: plain, slow,
-    obviously correct.  Returns (dq, dk, dv) as float64 arrays.
+    obviously correct.  ``heads``: optional list of (b, h) pairs to compute
+    (the gradients of every other head are left at zero), for checking a
+    sample of the heads of a large problem.  Returns (dq, dk, dv) as float64
+    arrays.
     """
     q, k, v, d_o = (_widen(x) for x in (q, k, v, d_o))
     B, H, S_q, D = q.shape
@@ -173,6 +176,8 @@ def attention_bwd_f64(q, k, v, d_o, scale: float, causal: bool, kv_valid_len=Non
         if causal:
             allowed = allowed & (j <= i)
         for h in range(H):
+            if heads is not None and (b, h) not in heads:
+                continue
             s = scale * (q[b, h] @ k[b, h].T)
             s = np.where(allowed, s, -np.inf)
             m = s.max(axis=1, keepdims=True)

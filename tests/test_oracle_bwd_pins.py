@@ -93,3 +93,17 @@ def test_backward_sums_and_masked_keys(causal):
         np.testing.assert_allclose(dv[b].sum(axis=1), g[b][:, has_key].sum(axis=1), atol=1e-12)
         assert np.all(dk[b, :, n:] == 0.0) and np.all(dv[b, :, n:] == 0.0)
     assert np.all(dq[2] == 0.0)
+
+
+def test_backward_head_subset_matches_full():
+    B, H, S, D = 2, 3, 10, 4
+    args = [draws(64, (B, H, S, D), t) for t in (1, 2, 3, 5)]
+    full = oracle.attention_bwd_f64(*args, 0.5, True, kv_valid_len=[10, 6])
+    part = oracle.attention_bwd_f64(*args, 0.5, True, kv_valid_len=[10, 6], heads=[(0, 2), (1, 0)])
+    for f, g in zip(full, part):
+        for b in range(B):
+            for h in range(H):
+                if (b, h) in [(0, 2), (1, 0)]:
+                    np.testing.assert_array_equal(g[b, h], f[b, h])
+                else:
+                    assert np.all(g[b, h] == 0.0)
