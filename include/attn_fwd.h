@@ -212,7 +212,8 @@ const char* attn_status_str(attn_status_t status);
  * attn_fwd_debug_status -- synchronise `stream`, then read and clear the
  * device status word that the kernels set when a bounded wait gives up.
  * Returns ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_DEVICE if the
- * synchronisation itself reported a CUDA error.
+ * synchronisation itself reported a CUDA error or the backward kernel found
+ * its dynamic shared memory off a 1024-byte boundary (it then runs nothing).
  */
 attn_status_t attn_fwd_debug_status(void* stream);
 

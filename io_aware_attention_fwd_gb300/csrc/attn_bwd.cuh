@@ -26,15 +26,14 @@
 //                       dV  += P^T dO_i             (TS: P^T from TMEM)
 //                       dK  += dS^T Q_i             (TS: dS^T from TMEM)
 //                       dQ_i = dS K_j               (SS: dS from shared memory,
-//                                                    into cols [128,128+D));
-//                                                    at D = 128 as dQ_i^T = K_j^T dS^T
-//                                                    (lanes = head dim, coalesced
-//                                                    reduction per query)
+//                                                    into cols [128,128+D))
 //       warps 4-7     one key row per thread: P^T and dS^T for the tile
 //                     (bf16, back into TMEM and, for dS, into shared memory);
 //                     at the end dK and dV out of TMEM into bf16 rows.
-//       warps 8-11    one query row per thread: dQ_i out of TMEM, reduce-added
-//                     into the fp32 accumulator.
+//       warps 8-11    one query row per thread: dQ_i out of TMEM into a
+//                     shared-memory staging buffer (two boxes of 32 fp32
+//                     columns per round), which one thread reduce-adds into
+//                     the fp32 accumulator with TMA bulk tensor reductions.
 //   attn_bwd_dq_convert  dQ = bf16(scale * accumulator).
 // TMEM: S^T | dP^T (then dQ_i) | dV | dK, 512 columns at D = 128.
 
@@ -53,12 +52,19 @@ struct BwdCfg {
   static constexpr int kDSOff = kDOOff + kTileBytes;           // dS^T [128 keys][128 queries] bf16
   static constexpr int kDSBytes = 128 * 128 * 2;
   static constexpr int kStatOff = kDSOff + kDSBytes;           // [2 tiles][lse2 | delta][128] fp32
-  static constexpr int kBarOff = kStatOff + 2 * 2 * 128 * 4;
+  // dQ staging for the TMA reduce-adds: 2 boxes of [128 rows x 32 fp32]
+  static constexpr int kStageOff = kStatOff + 2 * 2 * 128 * 4;
+  static constexpr int kStageBytes = 2 * 128 * 128;
+  static constexpr int kBarOff = kStageOff + kStageBytes;
   // kv_full | q_full[2] | q_empty[2] | do_full | do_empty | s_full | dp_full | p_ready |
-  // ds_ready | dq_full | dq_free | dsm_free | done | drain | stat[2]
-  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 + 9 + 2;
+  // ds_ready | dq_full | dq_free | dsm_free | done | drain | stat[2] | staged | stage_free
+  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 + 9 + 2 + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;      // [0] tmem base, [1] abort flag
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  // No alignment slack: the kernel checks that the dynamic shared memory
+  // starts on a 1024-byte boundary (it does when no static shared memory
+  // precedes it) and reports an error instead of running otherwise.
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static_assert(kStageOff % 1024 == 0, "swizzled staging boxes need 1024-byte alignment");
   static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
@@ -101,6 +107,9 @@ struct BwdSmem {
   __device__ uint32_t done() const { return bar(14); }
   __device__ uint32_t drain() const { return bar(15); }
   __device__ uint32_t stat(int b) const { return bar(16 + b); }
+  __device__ uint32_t staged() const { return bar(18); }
+  __device__ uint32_t stage_free() const { return bar(19); }
+  __device__ uint32_t stage() const { return base + BwdCfg<D>::kStageOff; }
 };
 
 // What one CTA covers: key tile j of head bh against query tiles
@@ -128,15 +137,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
-}
-
-__device__ __forceinline__ void red_add_f32(float* p, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
-}
-
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4_b32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -208,9 +208,6 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
   constexpr uint32_t idesc_s = make_idesc(kBM, kBN, false, false, false);  // [128 x 128], K-major A and B
   constexpr uint32_t idesc_acc = make_idesc(kBM, D, false, true, false);   // TS: B MN-major
   constexpr uint32_t idesc_dq = make_idesc(kBM, D, true, true, false);     // SS: A and B MN-major
-  // D = 128: dQ_i^T = K_j^T dS^T instead (lanes = head dim), so each warp's
-  // reduction into the accumulator covers 32 consecutive floats of a row
-  constexpr bool kDqT = (D == 128);
   const uint32_t leader = elect_one();
   const uint64_t kd = sdesc_kmajor_sw128(sm.k());
   const uint64_t vd = sdesc_kmajor_sw128(sm.v());
@@ -258,10 +255,7 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk) {
       const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
-      if (kDqT)
-        mma_ss_if<false>(leader, tDP, k_mn + off, ds_mn + off, idesc_dq, kk > 0 ? 1u : 0u);
-      else
-        mma_ss_if<false>(leader, tDP, ds_mn + off, k_mn + off, idesc_dq, kk > 0 ? 1u : 0u);
+      mma_ss_if<false>(leader, tDP, ds_mn + off, k_mn + off, idesc_dq, kk > 0 ? 1u : 0u);
     }
     tc_commit_if(leader, sm.dq_full());
     tc_commit_if(leader, sm.dsm_free());
@@ -418,55 +412,97 @@ __device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem,
   }
 }
 
-// Query rows (128 threads): dQ_i out of TMEM, reduce-added into the fp32 accumulator.
+// Query rows (128 threads): dQ_i out of TMEM into shared memory, then TMA
+// bulk reduce-adds of the tile into the fp32 accumulator.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 template <int D>
-__device__ void bwd_dq_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdParams& p, const BwdWork& wk,
-                            const WaitCtx& w) {
+__device__ void bwd_dq_role(const BwdSmem<D>& sm, const CUtensorMap* tmDQ, uint32_t tmem, const BwdParams& p,
+                            const BwdWork& wk, const WaitCtx& w) {
   using C = BwdCfg<D>;
   const int r = static_cast<int>(threadIdx.x) - 256;  // query row in the tile == TMEM lane
+  const bool leader = (r == 0);
   const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
   const uint32_t tQ = tmem + lane_off + C::kDPCol;
+  constexpr int kBoxes = D / 32;                  // 32 fp32 (128 B) per box row
+  constexpr int kBoxBytes = kBM * 128;            // one [128 rows x 32 fp32] box
+  if (leader) tma_prefetch_desc(tmDQ);
+  bool issued = false;
+  int nround = 0;  // staging rounds so far
   for (int t = 0; t < wk.n; ++t) {
     if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), t & 1, w))) break;
     tc_fence_after();
-    const int q0 = (wk.i0 + t) * kBM;
-    // read the whole tile row first and release its TMEM columns (the next
-    // dP^T product waits for them), then reduce into the accumulator
-    uint32_t a[128];
+    // read the whole row first and release its TMEM columns (the next dP^T
+    // product waits for them)
+    uint32_t a[D];
 #pragma unroll
-    for (int cc = 0; cc < (D == 128 ? 128 : D); cc += 32) tmem_ld32(tQ + cc, a + cc);
+    for (int cc = 0; cc < D; cc += 32) tmem_ld32(tQ + cc, a + cc);
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(sm.dq_free());
-    if constexpr (D == 128) {  // lane r holds dQ^T[r][query]: one coalesced row segment per warp per query
-      float* col = p.dq_acc + (static_cast<int64_t>(wk.bh) * p.S_q + q0) * D + r;
-      const int nq = min(kBM, p.S_q - q0);
+    // Stage row r in the layout of the accumulator's tensor-map boxes (box c:
+    // head-dim columns [32c, 32c + 32) of the 128 rows, 128 B per row, 16-byte
+    // chunks XOR-swizzled by row & 7, which also puts the 32 rows a warp
+    // writes at once in different banks), two boxes per round through the
+    // staging buffer; the leader reduce-adds each round into the accumulator
+    // and frees the buffer once the TMA has read it.
+    const int q0 = (wk.i0 + t) * kBM;
+    bool ok = true;
 #pragma unroll
-      for (int qq = 0; qq < 128; ++qq)
-        if (qq < nq) red_add_f32(col + static_cast<int64_t>(qq) * D, __uint_as_float(a[qq]));
-    } else {  // lane r holds dQ[query r][:]
-      const int q = q0 + r;
-      float* dst = p.dq_acc + (static_cast<int64_t>(wk.bh) * p.S_q + q) * D;
-      if (q < p.S_q) {
+    for (int rd = 0; rd < kBoxes / 2; ++rd) {
+      ok = __all_sync(0xffffffffu, nround == 0 || mbar_wait(sm.stage_free(), (nround - 1) & 1, w));
+      if (!ok) break;
 #pragma unroll
-        for (int e = 0; e < D; e += 4)
-          red_add_v4(dst + e, __uint_as_float(a[e]), __uint_as_float(a[e + 1]), __uint_as_float(a[e + 2]),
-                     __uint_as_float(a[e + 3]));
+      for (int cb = 0; cb < 2; ++cb) {
+        const int c = 2 * rd + cb;
+        const uint32_t box = sm.stage() + static_cast<uint32_t>(cb * kBoxBytes);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4_b32(box + static_cast<uint32_t>(r * 128 + ((k ^ (r & 7)) << 4)), a[32 * c + 4 * k],
+                           a[32 * c + 4 * k + 1], a[32 * c + 4 * k + 2], a[32 * c + 4 * k + 3]);
       }
+      fence_async_smem();
+      mbar_arrive(sm.staged());
+      if (leader) {  // rows past the head's last query fall outside the tensor map and are skipped
+        ok = mbar_wait(sm.staged(), nround & 1, w);
+        if (ok) {
+          tma_reduce_add_3d(tmDQ, sm.stage(), 64 * rd, q0, wk.bh);
+          tma_reduce_add_3d(tmDQ, sm.stage() + kBoxBytes, 64 * rd + 32, q0, wk.bh);
+          bulk_commit();
+          issued = true;
+          bulk_wait_read_all();  // the staging buffer has been read
+          mbar_arrive(sm.stage_free());
+        }
+      }
+      ++nround;
     }
+    if (!__all_sync(0xffffffffu, ok)) break;
   }
+  if (leader && issued) bulk_wait_all();  // the reductions are complete before the CTA exits
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t base = smem_u32(smem_raw);
+  if ((base & 1023u) != 0u) {  // the layout has no slack for realignment: report, run nothing
+    if (threadIdx.x == 0) atomicOr(&g_attn_status, 2u);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const BwdSmem<D> sm{base};
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
   const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -492,6 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sm.drain(), 1);
     mbar_init(sm.stat(0), kBM);
     mbar_init(sm.stat(1), kBM);
+    mbar_init(sm.staged(), kBM);
+    mbar_init(sm.stage_free(), 1);
     misc[1] = 0u;
     fence_barrier_init();
   }
@@ -512,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4 && warp < 8) {
     bwd_row_role<D>(sm, smem, tmem, p, wk, w);
   } else if (warp >= 8) {
-    bwd_dq_role<D>(sm, tmem, p, wk, w);
+    bwd_dq_role<D>(sm, &tmDQ, tmem, p, wk, w);
   }
 
   tc_fence_before();

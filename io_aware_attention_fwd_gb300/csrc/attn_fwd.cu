@@ -118,7 +118,9 @@ struct Params {
 
 }  // namespace
 
-// Set by a bounded wait that gave up; read and cleared by attn_fwd_debug_status.
+// Read and cleared by attn_fwd_debug_status.  Bit 0: a bounded wait gave up.
+// Bit 1: the backward kernel found its dynamic shared memory off a 1024-byte
+// boundary and ran nothing.
 __device__ unsigned int g_attn_status = 0;
 
 namespace {
@@ -1056,7 +1058,10 @@ bool encode_3d(CUtensorMap* m, const void* ptr, int D, int S, int64_t BH, int eb
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * eb, static_cast<cuuint64_t>(S) * D * eb};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return g_encode(m, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+  const CUtensorMapDataType dt = eb == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return g_encode(m, dt, 3,
                   const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1196,9 +1201,9 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   attn_bwd_prep<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_o), lse, lse2, delta, dq_acc, S_q, S_pad, BH);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!encode_3d(&tq, q, D, S_q, BH) || !encode_3d(&tk, k, D, S_kv, BH) || !encode_3d(&tv, v, D, S_kv, BH) ||
-      !encode_3d(&tdo, d_o, D, S_q, BH))
+      !encode_3d(&tdo, d_o, D, S_q, BH) || !encode_3d(&tdq, dq_acc, D, S_q, BH, 4))
     return ATTN_ERR_LAUNCH;
   BwdParams prm;
   prm.dq_acc = dq_acc;
@@ -1219,7 +1224,7 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   prm.causal = causal;
   prm.timeout_ns = kDefaultTimeoutNs;
   const int64_t grid = BH * prm.n_kv_tiles;
-  attn_bwd_sm103a<D><<<static_cast<unsigned>(grid), kThreads, BwdCfg<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, prm);
+  attn_bwd_sm103a<D><<<static_cast<unsigned>(grid), kThreads, BwdCfg<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   const int64_t n4 = BH * S_q * D / 4;
   const int64_t cv_blocks = std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(sms) * 16);
@@ -1475,6 +1480,7 @@ attn_status_t attn_fwd_debug_status(void* stream) {
   unsigned int word = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&word, g_attn_status, sizeof word) != cudaSuccess) return ATTN_ERR_DEVICE;
   if (word != 0u && cudaMemcpyToSymbol(g_attn_status, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_DEVICE;
+  if (word & 2u) return ATTN_ERR_DEVICE;  // a kernel found its shared memory misaligned and did not run
   return word != 0u ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
