@@ -279,3 +279,33 @@ def test_merge_closed_forms():
     o, l = oracle.merge_f64([o1], [[0.25, 7.0]])
     np.testing.assert_array_equal(o, o1)
     np.testing.assert_array_equal(l, [0.25, 7.0])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_matches_extended_precision_brute_force(causal):
+    """Tiny problems (S <= 16) evaluated directly in numpy's long double, one
+    sum at a time: the score of every allowed pair, the row maximum, the
+    exponentials, their sum and the weighted sum of value rows."""
+    B, H, S_q, S_kv, D = 2, 2, 9, 13, 8
+    q = bits(71, (B, H, S_q, D), si.TID_Q, 2.0)
+    k = bits(71, (B, H, S_kv, D), si.TID_K, 2.0)
+    v = bits(71, (B, H, S_kv, D), si.TID_V)
+    valid = [13, 5]
+    scale = 0.35
+    o, lse = oracle.attention_f64(q, k, v, scale, causal, kv_valid_len=valid)
+    o = o.reshape(B, H, S_q, D)
+    lse = lse.reshape(B, H, S_q)
+    ld = np.longdouble
+    ql, kl, vl = (si.bf16_bits_to_f32(x).astype(ld) for x in (q, k, v))
+    for b in range(B):
+        for h in range(H):
+            for i in range(S_q):
+                allowed = [j for j in range(S_kv) if j < valid[b] and (not causal or j <= i)]
+                s = {j: ld(scale) * sum(ql[b, h, i, d] * kl[b, h, j, d] for d in range(D)) for j in allowed}
+                m = max(s.values())
+                e = {j: np.exp(s[j] - m) for j in allowed}
+                l = sum(e.values())
+                ref_o = [sum(e[j] * vl[b, h, j, d] for j in allowed) / l for d in range(D)]
+                ref_lse = m + np.log(l)
+                assert np.allclose(o[b, h, i].astype(ld), ref_o, rtol=0, atol=1e-12), (b, h, i)
+                assert abs(ld(lse[b, h, i]) - ref_lse) <= 1e-12, (b, h, i)
