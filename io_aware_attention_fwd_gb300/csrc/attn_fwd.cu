@@ -83,7 +83,9 @@ struct Cfg {
   static constexpr int kKeysPerStep = 32 / kEB;       // keys per P.V MMA K step
   static constexpr int kPvSteps = kBN / kKeysPerStep;
   static constexpr int kPCols = kBN * kEB / 4;        // TMEM columns of packed P
-  static constexpr int kSlots = kF8 ? 12 : ((D == 128) ? 5 : 12);
+  // K/V ring depth.  At D = 64 a shallow ring measured best: all CTAs start
+  // together and a deep ring makes them all ask DRAM for many tiles at once.
+  static constexpr int kSlots = kF8 ? 12 : ((D == 128) ? 5 : 4);
   static constexpr bool kTurn = !kF8 && D == 128;  // softmax warpgroups alternate
   static constexpr int kQOff = 0;
   static constexpr int kSlotOff = kQTiles * kTileBytes;
