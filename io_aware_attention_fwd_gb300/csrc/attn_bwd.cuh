@@ -30,6 +30,10 @@
 //       warps 4-7     one key row per thread: P^T and dS^T for the tile
 //                     (bf16, back into TMEM and, for dS, into shared memory);
 //                     at the end dK and dV out of TMEM into bf16 rows.
+//                     At D = 64 warps 8-11 form a second such warpgroup: each
+//                     takes 64 of the tile's query columns and half of dQ,
+//                     dK and dV (bwd_row_role2), and there is no separate dQ
+//                     warpgroup.
 //       warps 8-11    one query row per thread: dQ_i out of TMEM into a
 //                     shared-memory staging buffer (two boxes of 32 fp32
 //                     columns per round), which one thread reduce-adds into
@@ -57,8 +61,9 @@ struct BwdCfg {
   static constexpr int kStageBytes = 2 * 128 * 128;
   static constexpr int kBarOff = kStageOff + kStageBytes;
   // kv_full | q_full[2] | q_empty[2] | do_full | do_empty | s_full | dp_full | p_ready |
-  // ds_ready | dq_full | dq_free | dsm_free | done | drain | stat[2] | staged | stage_free
-  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 + 9 + 2 + 2;
+  // ds_ready | dq_full | dq_free | dsm_free | done | drain | stat[2] | staged | stage_free |
+  // stat2[2] | staged2 | stage_free2 (the second key-row warpgroup)
+  static constexpr int kNumBars = 1 + 2 * kQSlots + 2 + 9 + 2 + 2 + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;      // [0] tmem base, [1] abort flag
   // No alignment slack: the kernel checks that the dynamic shared memory
   // starts on a 1024-byte boundary (it does when no static shared memory
@@ -66,6 +71,9 @@ struct BwdCfg {
   static constexpr int kSmemBytes = kMiscOff + 16;
   static_assert(kStageOff % 1024 == 0, "swizzled staging boxes need 1024-byte alignment");
   static constexpr uint32_t kSCol = 0, kDPCol = 128, kDVCol = 256, kDKCol = 256 + D;
+  // D = 64: two key-row warpgroups, each taking 64 of the 128 query columns
+  // (and half of the dQ reduction); D = 128: one, plus a dQ warpgroup.
+  static constexpr int kRowWGs = (D == 64) ? 2 : 1;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -110,6 +118,10 @@ struct BwdSmem {
   __device__ uint32_t staged() const { return bar(18); }
   __device__ uint32_t stage_free() const { return bar(19); }
   __device__ uint32_t stage() const { return base + BwdCfg<D>::kStageOff; }
+  // per key-row warpgroup h (kRowWGs = 2): statistics, staging handshake
+  __device__ uint32_t stat_h(int h, int b) const { return h ? bar(20 + b) : stat(b); }
+  __device__ uint32_t staged_h(int h) const { return h ? bar(22) : staged(); }
+  __device__ uint32_t stage_free_h(int h) const { return h ? bar(23) : stage_free(); }
 };
 
 // What one CTA covers: key tile j of head bh against query tiles
@@ -148,10 +160,10 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 
 // One key row of P^T for a query tile: p = 2^(c s - lse2) for its 128 query
 // columns, packed to bf16 pairs.  kMask: column col is allowed iff col >= first.
-template <bool kMask>
+template <bool kMask, int kN = 128>
 __device__ __forceinline__ void bwd_p_row(const uint32_t* sr, const float* st, float c, int first, uint32_t* pk) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {  // four queries at a time
+  for (int i = 0; i < kN / 4; ++i) {  // four queries at a time
     const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * i);
     const float lse2[4] = {l4.x, l4.y, l4.z, l4.w};
     float pv[4];
@@ -163,6 +175,22 @@ __device__ __forceinline__ void bwd_p_row(const uint32_t* sr, const float* st, f
     }
     pk[2 * i] = pack_bf16x2(pv[0], pv[1]);
     pk[2 * i + 1] = pack_bf16x2(pv[2], pv[3]);
+  }
+}
+
+// acc[tmem] (+)= A[tmem] . B[smem] over the 128 queries of a tile: the TS
+// products dV += P^T dO and dK += dS^T Q.  Every MMA consumes 16 queries (8
+// packed TMEM columns of A).  With two key-row warpgroups, the packed columns
+// of queries 64-127 start at column 64 (each warpgroup packs in place over its
+// own score columns).
+template <int D>
+__device__ __forceinline__ void bwd_issue_ts(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBM / 16; ++kk) {
+    const uint32_t a_col = (BwdCfg<D>::kRowWGs == 2) ? (kk >> 2) * 64 + (kk & 3) * 8 : kk * 8;
+    mma_ts_if<false>(pred, d_tmem, a_tmem + a_col, b_desc + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
+                     (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -237,7 +265,7 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
     ok = __all_sync(0xffffffffu, mbar_wait(sm.p_ready(), t & 1, w));
     if (!ok) break;
     tc_fence_after();
-    issue_pv<D, false>(leader, tDV, tS, do_mn, idesc_acc, t > 0);
+    bwd_issue_ts<D>(leader, tDV, tS, do_mn, idesc_acc, t > 0);
     tc_commit_if(leader, sm.do_empty());
     if (t + 1 < wk.n) {  // S^T_{t+1}
       const int qn = (t + 1) % C::kQSlots;
@@ -251,7 +279,7 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
     ok = __all_sync(0xffffffffu, mbar_wait(sm.ds_ready(), t & 1, w));
     if (!ok) break;
     tc_fence_after();
-    issue_pv<D, false>(leader, tDK, tDP, q_mn, idesc_acc, t > 0);
+    bwd_issue_ts<D>(leader, tDK, tDP, q_mn, idesc_acc, t > 0);
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk) {
       const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
@@ -425,6 +453,175 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Key rows with two warpgroups (D = 64): warpgroup hf takes query columns
+// [64 hf, 64 hf + 64) of every tile -- P^T and dS^T need no row-wide
+// statistic, only LSE and Delta, so the halves never talk to each other --
+// and head-dim columns [32 hf, 32 hf + 32) of dQ (one tensor-map box each,
+// staged and reduce-added by the warpgroup itself), dK and dV.  dQ_t is read
+// out at the start of tile t + 1, before P^T of that tile, so the next dP^T
+// product can start while the exponentials run.
+template <int D>
+__device__ void bwd_row_role2(const BwdSmem<D>& sm, uint8_t* smem, const CUtensorMap* tmDQ, uint32_t tmem,
+                              const BwdParams& p, const BwdWork& wk, const WaitCtx& w, int hf) {
+  using C = BwdCfg<D>;
+  static_assert(C::kRowWGs == 2 && D == 64, "two key-row warpgroups: D = 64");
+  constexpr int kN = 64;  // query columns of this warpgroup
+  const int r = static_cast<int>(((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31));  // key row == TMEM lane
+  const bool leader = (r == 0);
+  const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_off + C::kSCol + hf * kN;    // this half's S^T / P^T columns
+  const uint32_t tDP = tmem + lane_off + C::kDPCol + hf * kN;  // this half's dP^T / dS^T columns
+  const uint32_t tQ = tmem + lane_off + C::kDPCol + hf * 32;   // dQ_t: row r, this half's 32 head-dim columns
+  const int key = wk.k0 + r;
+  const bool key_ok = key < wk.nk_pad;
+  const float c = p.scale_log2;
+  // statistics: [2 tiles][64 lse2 | 64 delta] per warpgroup
+  float* stats = reinterpret_cast<float*>(smem + C::kStatOff) + hf * 256;
+  const uint32_t box = sm.stage() + static_cast<uint32_t>(hf * kBM * 128);  // this half's dQ staging box
+  if (leader) tma_prefetch_desc(tmDQ);
+  bool ok = true, issued = false;
+  // thread r loads lse2 (r < 64) or delta (r >= 64) of query 64 hf + (r & 63), one tile ahead
+  const float* src = (r < 64) ? p.lse2 : p.delta;
+  const int64_t srow0 = static_cast<int64_t>(wk.bh) * p.S_pad + wk.i0 * kBM + hf * kN + (r & 63);
+  float next_v = (wk.n > 0) ? __ldg(src + srow0) : 0.f;
+  int nstaged = 0;
+  // dQ of tile tt (this half's columns) out of TMEM, staged, and reduce-added
+  auto reduce_dq = [&](int tt) -> bool {
+    if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), tt & 1, w))) return false;
+    tc_fence_after();
+    uint32_t a[32];
+    tmem_ld32(tQ, a);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(sm.dq_free());
+    if (nstaged > 0) {  // the previous reduction of this box has read it
+      if (leader) {
+        bulk_wait_read_all();
+        mbar_arrive(sm.stage_free_h(hf));
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(sm.stage_free_h(hf), (nstaged - 1) & 1, w))) return false;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      st_shared_v4_b32(box + static_cast<uint32_t>(r * 128 + ((k ^ (r & 7)) << 4)), a[4 * k], a[4 * k + 1],
+                       a[4 * k + 2], a[4 * k + 3]);
+    fence_async_smem();
+    mbar_arrive(sm.staged_h(hf));
+    if (leader) {  // rows past the head's last query fall outside the tensor map and are skipped
+      if (!mbar_wait(sm.staged_h(hf), nstaged & 1, w)) return false;
+      tma_reduce_add_3d(tmDQ, box, 32 * hf, (wk.i0 + tt) * kBM, wk.bh);
+      bulk_commit();
+      issued = true;
+    }
+    ++nstaged;
+    return true;
+  };
+  for (int t = 0; t < wk.n && ok; ++t) {
+    const int q0 = (wk.i0 + t) * kBM;
+    float* st = stats + (t & 1) * 128;  // [lse2 | delta] of this tile's 64 columns
+    st[(r < 64 ? 0 : 64) + (r & 63)] = next_v;
+    if (t + 1 < wk.n) next_v = __ldg(src + srow0 + (t + 1) * kBM);
+    mbar_arrive(sm.stat_h(hf, t & 1));
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.stat_h(hf, t & 1), (t >> 1) & 1, w));
+    if (!ok) break;
+    if (t > 0 && !reduce_dq(t - 1)) {
+      ok = false;
+      break;
+    }
+
+    // P^T row: p_c = 2^(c*s_c - lse2_c) for the allowed (key, query) pairs
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.s_full(), t & 1, w));
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t sr[kN];
+    tmem_ld32(tS + 0, sr + 0);
+    tmem_ld32(tS + 32, sr + 32);
+    tmem_wait_ld();
+    const int qh = q0 + hf * kN;  // this half's first query
+    const bool diag = p.causal && qh < wk.k0 + kBN;
+    uint32_t pk[kN / 2];
+    if (diag || wk.k0 + kBN > wk.nk_pad) {
+      const int first = !key_ok ? kN : (diag ? key - qh : 0);
+      bwd_p_row<true, kN>(sr, st, c, first, pk);
+    } else {
+      bwd_p_row<false, kN>(sr, st, c, 0, pk);
+    }
+    tmem_st32(tS, pk);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(sm.p_ready());
+
+    // dS^T row: p * (dP^T - delta), to TMEM (for dK) and shared memory (for dQ)
+    ok = __all_sync(0xffffffffu, mbar_wait(sm.dp_full(), t & 1, w));
+    if (ok && t > 0) ok = __all_sync(0xffffffffu, mbar_wait(sm.dsm_free(), (t - 1) & 1, w));
+    if (!ok) break;
+    tc_fence_after();
+#pragma unroll
+    for (int cc = 0; cc < kN; cc += 32) {
+      uint32_t dpr[32];
+      tmem_ld32(tDP + cc, dpr);
+      tmem_wait_ld();
+      uint32_t dsw[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // four queries at a time
+        const float4 d4 = *reinterpret_cast<const float4*>(st + 64 + cc + 4 * i);
+        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t pw = pk[(cc >> 1) + 2 * i + h];
+          const float p0 = __uint_as_float(pw << 16), p1 = __uint_as_float(pw & 0xFFFF0000u);
+          const float d0 = p0 * (__uint_as_float(dpr[4 * i + 2 * h]) - dl[2 * h]);
+          const float d1 = p1 * (__uint_as_float(dpr[4 * i + 2 * h + 1]) - dl[2 * h + 1]);
+          dsw[2 * i + h] = pack_bf16x2(d0, d1);
+        }
+      }
+      tmem_st16(tDP + (cc >> 1), dsw);
+      // shared memory: row r of the [key][query] tile, panel hf (queries 64 hf ..), 128-byte swizzle
+      const uint32_t row = sm.ds() + static_cast<uint32_t>(hf * kPanelBytes + r * 128);
+      const int chunk0 = cc >> 3;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        st_shared_v4_b32(row + static_cast<uint32_t>(((chunk0 + u) ^ (r & 7)) << 4), dsw[4 * u], dsw[4 * u + 1],
+                         dsw[4 * u + 2], dsw[4 * u + 3]);
+    }
+    tmem_wait_st();
+    fence_async_smem();
+    tc_fence_before();
+    mbar_arrive(sm.ds_ready());
+  }
+  if (ok && wk.n > 0) ok = reduce_dq(wk.n - 1);
+  if (leader && issued) bulk_wait_all();  // the reductions are complete before the CTA exits
+
+  // this half's head-dim columns of the dK and dV rows (zero when the CTA had no work)
+  bool have = ok && wk.n > 0;
+  if (have) have = __all_sync(0xffffffffu, mbar_wait(sm.done(), 0, w));
+  if (have) tc_fence_after();
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (times scale)
+    const uint32_t srcc = tmem + lane_off + (which ? C::kDKCol : C::kDVCol) + hf * 32;
+    uint16_t* dst = (which ? p.dk : p.dv) + (static_cast<int64_t>(wk.bh) * p.S_kv + key) * D + hf * 32;
+    const float f = which ? p.scale : 1.f;
+    uint32_t a[32];
+    if (have) {
+      tmem_ld32(srcc, a);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a[i] = 0u;
+    }
+    if (key < p.S_kv) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          wv[e] = pack_bf16x2(__uint_as_float(a[8 * q + 2 * e]) * f, __uint_as_float(a[8 * q + 2 * e + 1]) * f);
+        st_global_v4(dst + 8 * q, wv[0], wv[1], wv[2], wv[3]);
+      }
+    }
+  }
+}
+
 template <int D>
 __device__ void bwd_dq_role(const BwdSmem<D>& sm, const CUtensorMap* tmDQ, uint32_t tmem, const BwdParams& p,
                             const BwdWork& wk, const WaitCtx& w) {
@@ -519,10 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sm.do_empty(), 1);
     mbar_init(sm.s_full(), 1);
     mbar_init(sm.dp_full(), 1);
-    mbar_init(sm.p_ready(), kBM);
-    mbar_init(sm.ds_ready(), kBM);
+    mbar_init(sm.p_ready(), kBM * C::kRowWGs);
+    mbar_init(sm.ds_ready(), kBM * C::kRowWGs);
     mbar_init(sm.dq_full(), 1);
-    mbar_init(sm.dq_free(), kBM);
+    mbar_init(sm.dq_free(), kBM * C::kRowWGs);
     mbar_init(sm.dsm_free(), 1);
     mbar_init(sm.done(), 1);
     mbar_init(sm.drain(), 1);
@@ -530,6 +727,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sm.stat(1), kBM);
     mbar_init(sm.staged(), kBM);
     mbar_init(sm.stage_free(), 1);
+    for (int h = 0; h < 2; ++h) mbar_init(sm.stat_h(1, h), kBM);
+    mbar_init(sm.staged_h(1), kBM);
+    mbar_init(sm.stage_free_h(1), 1);
     misc[1] = 0u;
     fence_barrier_init();
   }
@@ -547,10 +747,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && wk.n > 0) bwd_load_role<D>(sm, &tmQ, &tmK, &tmV, &tmDO, wk, w);
   } else if (warp == 1) {
     if (wk.n > 0) bwd_mma_role<D>(sm, tmem, wk, w);
-  } else if (warp >= 4 && warp < 8) {
-    bwd_row_role<D>(sm, smem, tmem, p, wk, w);
-  } else if (warp >= 8) {
-    bwd_dq_role<D>(sm, &tmDQ, tmem, p, wk, w);
+  } else if (warp >= 4) {
+    if constexpr (C::kRowWGs == 2) {
+      bwd_row_role2<D>(sm, smem, &tmDQ, tmem, p, wk, w, (warp - 4) >> 2);
+    } else if (warp < 8) {
+      bwd_row_role<D>(sm, smem, tmem, p, wk, w);
+    } else {
+      bwd_dq_role<D>(sm, &tmDQ, tmem, p, wk, w);
+    }
   }
 
   tc_fence_before();
