@@ -158,8 +158,8 @@ __device__ __forceinline__ void st_shared_v4_b32(uint32_t addr, uint32_t a, uint
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// One key row of P^T for a query tile: p = 2^(c s - lse2) for its 128 query
-// columns, packed to bf16 pairs.  kMask: column col is allowed iff col >= first.
+// One key row of P^T for kN query columns of a tile: p = 2^(c s - lse2),
+// packed to bf16 pairs.  kMask: column col is allowed iff col >= first.
 template <bool kMask, int kN = 128>
 __device__ __forceinline__ void bwd_p_row(const uint32_t* sr, const float* st, float c, int first, uint32_t* pk) {
 #pragma unroll
@@ -344,23 +344,25 @@ __device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem,
     ok = __all_sync(0xffffffffu, mbar_wait(sm.s_full(), t & 1, w));
     if (!ok) break;
     tc_fence_after();
-    uint32_t sr[128];
-    tmem_ld32(tS + 0, sr + 0);
-    tmem_ld32(tS + 32, sr + 32);
-    tmem_ld32(tS + 64, sr + 64);
-    tmem_ld32(tS + 96, sr + 96);
-    tmem_wait_ld();
     // Masking only on tiles that need it (the causal diagonal, or padded
     // keys): query column col is allowed iff col >= first, and a masked score
     // enters the exponential as -inf, so its P is exactly 0.  Both loops run
-    // without a branch per score.
+    // without a branch per score.  The row is read in two halves of 64
+    // columns: a whole row (128 registers) next to the packed P would spill.
     const bool diag = p.causal && q0 < wk.k0 + kBN;  // some query of the tile precedes some key
+    const bool masked = diag || wk.k0 + kBN > wk.nk_pad;
+    const int first = !key_ok ? kBM : (diag ? key - q0 : 0);
     uint32_t pk[64];
-    if (diag || wk.k0 + kBN > wk.nk_pad) {
-      const int first = !key_ok ? kBM : (diag ? key - q0 : 0);
-      bwd_p_row<true>(sr, st, c, first, pk);
-    } else {
-      bwd_p_row<false>(sr, st, c, 0, pk);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t sr[64];
+      tmem_ld32(tS + hh * 64, sr);
+      tmem_ld32(tS + hh * 64 + 32, sr + 32);
+      tmem_wait_ld();
+      if (masked)
+        bwd_p_row<true, 64>(sr, st + hh * 64, c, first - hh * 64, pk + hh * 32);
+      else
+        bwd_p_row<false, 64>(sr, st + hh * 64, c, 0, pk + hh * 32);
     }
     tmem_st32(tS + 0, pk + 0);
     tmem_st32(tS + 32, pk + 32);
