@@ -116,15 +116,17 @@ def test_bwd_allocates_only_its_workspace(dev):
     assert torch.cuda.mem_get_info(dev)[0] == free0
 
 
+@pytest.mark.parametrize("shape", ["b1_h32_s8192_d128", "b4_h16_s1024_d64"])
 @pytest.mark.parametrize("causal", [True, False])
-def test_bwd_bench_size_sampled_heads(dev, causal):
-    """The backward workload the benchmark times (B=1, H=32, S=8192, D=128,
-    seed 8, inputs drawn on the device, one attn_bwd call over all heads),
-    checked on two seeded heads against the oracle's full gradients of those
-    heads."""
+def test_bwd_bench_size_sampled_heads(dev, causal, shape):
+    """The backward workloads the benchmark times (B=1, H=32, S=8192, D=128
+    and B=4, H=16, S=1024, D=64; seed 8, inputs drawn on the device, one
+    attn_bwd call over all heads), checked on two seeded heads against the
+    oracle's full gradients of those heads."""
     import torch
     import io_aware_attention_fwd_gb300 as attn
-    B, H, S, D, seed = 1, 32, 8192, 128, 8
+    B, H, S, D = {"b1_h32_s8192_d128": (1, 32, 8192, 128), "b4_h16_s1024_d64": (4, 16, 1024, 64)}[shape]
+    seed = 8
     scale = 1 / math.sqrt(D)
     q, k, v = si.qkv_bf16_torch(seed, B, H, S, S, D, device=dev)
     d_o = si.normal_bf16_torch(seed, 5, B * H * S * D, device=dev).view(B, H, S, D)
@@ -137,8 +139,11 @@ def test_bwd_bench_size_sampled_heads(dev, causal):
     attn.attn_bwd(q, k, v, o, lse, d_o, dq, dk, dv, B, H, S, S, D, scale, causal, None, ws, nbytes)
     torch.cuda.synchronize()
     assert attn.attn_fwd_debug_status() == attn.ATTN_OK
-    heads = [int(x) for x in si.sample_rows(seed * 7 + int(causal), H, 2, must_include=())]
-    bits = lambda t: t[:, heads].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    ref = oracle.attention_bwd_f64(bits(q), bits(k), bits(v), bits(d_o), scale, causal)
-    got = [x[:, heads].float().cpu().numpy().astype(np.float64) for x in (dq, dk, dv)]
-    compare_grads(got, ref)
+    # two seeded (batch, head) pairs; the first batch always included
+    picks = [int(x) for x in si.sample_rows(seed * 7 + int(causal), B * H, 2, must_include=(0,))]
+    for bh in picks:
+        b, h = divmod(bh, H)
+        bits = lambda t: t[b:b + 1, h:h + 1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        ref = oracle.attention_bwd_f64(bits(q), bits(k), bits(v), bits(d_o), scale, causal)
+        got = [x[b:b + 1, h:h + 1].float().cpu().numpy().astype(np.float64) for x in (dq, dk, dv)]
+        compare_grads(got, ref)

@@ -100,6 +100,30 @@ def test_fp8_8k_sampled_rows(dev):
         check(q8, k8, v8, 1 / math.sqrt(128), (1 / 16, 1 / 16, 1 / 16), causal, rows=rows)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_fp8_bench_size_32k_sampled_rows(dev, causal):
+    """The e4m3 workload the benchmark times at 32k (B=1, H=32, S=32768,
+    D=128, seed 6, N(0,1) x 16 rounded to e4m3 on the device, descales 1/16,
+    one launch over all heads), checked on seeded rows of every head,
+    including the first and last positions."""
+    import torch
+    import io_aware_attention_fwd_gb300 as attn
+    B, H, S, D, seed, m8 = 1, 32, 32768, 128, 6, 16.0
+    q, k, v = (si.normal_e4m3_torch(seed, tid, B * H * S * D, m8, device=dev).view(B, H, S, D)
+               for tid in (si.TID_Q, si.TID_K, si.TID_V))
+    o = torch.empty((B, H, S, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    scale, d8 = 1 / math.sqrt(D), 1 / m8
+    attn.attn_fwd_fp8(q, k, v, o, lse, B, H, S, S, D, scale, d8, d8, d8, causal, None)
+    torch.cuda.synchronize()
+    assert attn.attn_fwd_debug_status() == attn.ATTN_OK
+    rows = parity.sampled_rows(seed * 3 + int(causal), B, H, S, 8, must_include=[0, S // 2, S - 1])
+    og, lg = parity.gather_rows(o, lse, rows)
+    host = [x.view(torch.uint8).cpu().numpy() for x in (q, k, v)]
+    o_ref, l_ref = oracle_fp8(*host, scale, (d8, d8, d8), causal, rows=rows)
+    parity.compare(og, lg, o_ref, l_ref, FP8_MAX_ABS, FP8_REL_RMS, FP8_LSE_ABS)
+
+
 def test_fp8_close_to_bf16_path_on_the_same_values(dev):
     # the same (e4m3-representable) values through the bf16 kernel: the two
     # differ only by P's rounding (e4m3 vs bf16)
