@@ -1,7 +1,7 @@
 """Helpers shared by the GPU parity tests: upload seeded inputs, run the CUDA
 path through the C ABI, and compare with the fp64 oracle on the same rows.
 
-Tolerances (fixed by the task's parity bar): bf16 O within max-abs 2e-2 and
+Tolerances (the parity bar): bf16 O within max-abs 2e-2 and
 relative RMS 1e-2 of the oracle; fp32 LSE within 1e-3 absolute.  A row with
 no allowed key must give O = 0 and LSE = -inf on both sides.
 """
