@@ -53,6 +53,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "attn_fwd.h"
 
@@ -961,16 +962,21 @@ __global__ void attn_fill_empty(uint16_t* o, float* lse, int64_t rows, int D) {
 // key splitting, and the per-device combine step of ring attention
 // ("Flash attention" glossary page, paragraph 4):
 //   lse = ln sum_k exp(lse_k),   O = sum_k exp(lse_k - lse) O_k.
-// One warp per row; each lane owns D/32 consecutive columns.  A part with
-// lse_k = -inf (no keys) has weight 0; a row where every part has -inf gets
-// O = 0 and LSE = -inf.  HBM-bound: n_parts * (D + 1) * 4 bytes read and
-// D * 2 + 4 bytes written per row.
+// One warp per row; each lane owns D/32 consecutive columns.  Lane j holds
+// the weight of part k0 + j of each group of 32 parts and hands it to the
+// warp by shuffle; the partial rows are read eight at a time with
+// independent loads, so the warp waits for memory once per eight parts, not
+// once per part.  A part with lse_k = -inf (no keys) has weight 0; a row
+// where every part has -inf gets O = 0 and LSE = -inf.  HBM-bound:
+// n_parts * (D + 1) * 4 bytes read and D * 2 + 4 bytes written per row.
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict__ o_parts,
                                                          const float* __restrict__ lse_parts, int n_parts,
                                                          int64_t rows, int64_t part_stride_rows,
                                                          uint16_t* __restrict__ o, float* __restrict__ lse) {
-  constexpr int kPer = D / 32;
+  constexpr int kPer = D / 32;  // 4 (float4 per lane) or 2 (float2)
+  constexpr int kBatch = 8;     // partial rows in flight per warp
+  using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
   const int lane = static_cast<int>(threadIdx.x & 31);
   const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t step = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -982,26 +988,38 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    float wsum = 0.f;
+    float wsum = 0.f;  // this lane's share of the weight sum
     if (mx > -INFINITY) {
-      for (int k = 0; k < n_parts; ++k) {
-        const int64_t pr = k * part_stride_rows + row;
-        const float wk = expf(__ldg(lse_parts + pr) - mx);
-        wsum += wk;
-        const float* src = o_parts + pr * D + lane * kPer;
-        if (kPer == 4) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(src));
-          acc[0] += wk * v.x;
-          acc[1] += wk * v.y;
-          acc[2 % kPer] += wk * v.z;
-          acc[3 % kPer] += wk * v.w;
-        } else {
-          const float2 v = __ldg(reinterpret_cast<const float2*>(src));
-          acc[0] += wk * v.x;
-          acc[1] += wk * v.y;
+      const float* src = o_parts + row * D + lane * kPer;
+      for (int k0 = 0; k0 < n_parts; k0 += 32) {
+        const int cnt = min(32, n_parts - k0);
+        const float w_mine = lane < cnt ? expf(__ldg(lse_parts + (k0 + lane) * part_stride_rows + row) - mx) : 0.f;
+        wsum += w_mine;
+        int j = 0;
+        for (; j + kBatch <= cnt; j += kBatch) {
+          Vec v[kBatch];
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u)
+            v[u] = __ldg(reinterpret_cast<const Vec*>(src + (k0 + j + u) * part_stride_rows * D));
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const float wk = __shfl_sync(0xffffffffu, w_mine, j + u);
+            const float* f = reinterpret_cast<const float*>(&v[u]);
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[e] += wk * f[e];
+          }
+        }
+        for (; j < cnt; ++j) {
+          const Vec v = __ldg(reinterpret_cast<const Vec*>(src + (k0 + j) * part_stride_rows * D));
+          const float wk = __shfl_sync(0xffffffffu, w_mine, j);
+          const float* f = reinterpret_cast<const float*>(&v);
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) acc[e] += wk * f[e];
         }
       }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     uint32_t packed[kPer / 2];
 #pragma unroll
