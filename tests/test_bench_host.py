@@ -45,6 +45,23 @@ def _worker(rank, world, port, out):
     dist.destroy_process_group()
 
 
+@pytest.mark.parametrize("B,H", [(4, 16), (1, 32), (2, 32), (1, 2), (1, 1), (3, 5), (8, 2)])
+def test_e2e_pieces_cover_the_grid_once_contiguously(B, H):
+    # the end-to-end leg moves each piece with one copy per tensor and runs it
+    # as one attn_fwd call: whole batches, or a head range of one batch
+    seen = set()
+    pieces = bench.e2e_chunks(B, H)
+    for b0, nb, h0, nh in pieces:
+        assert nb >= 1 and nh >= 1
+        assert nb == 1 or (h0 == 0 and nh == H)
+        for b in range(b0, b0 + nb):
+            for h in range(h0, h0 + nh):
+                assert (b, h) not in seen
+                seen.add((b, h))
+    assert len(seen) == B * H
+    assert len(pieces) <= max(4, B * 2)
+
+
 def test_rank_aggregation_gloo_world2():
     import torch.multiprocessing as mp
     ctx = mp.get_context("spawn")
