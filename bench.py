@@ -110,19 +110,6 @@ def alg_bytes(w, causal):
     return H * (2 * S * D * 2 * B + 2 * kv * D * 2 + S * 4 * B)
 
 
-def e2e_chunks(B, H, target=4):
-    """Slices of the [B][H] grid for the end-to-end leg: about ``target``
-    contiguous pieces, each either whole batches (b0, nb, 0, H) or a head range
-    of one batch (b, 1, h0, nh), so every piece of a [B][H][S][D] tensor is
-    one contiguous block and one ordinary attn_fwd call."""
-    if B >= target:
-        nb = -(-B // target)
-        return [(b0, min(nb, B - b0), 0, H) for b0 in range(0, B, nb)]
-    per_b = -(-target // B)                  # head pieces per batch
-    nh = -(-H // per_b)
-    return [(b, 1, h0, min(nh, H - h0)) for b in range(B) for h0 in range(0, H, nh)]
-
-
 def aggregate_ranks(flops_step, t_step_ms, t_e2e_ms, dist=None, device="cpu"):
     """Whole-job numbers over all ranks: (value, e2e value, max step ms, max e2e ms).
 
@@ -424,64 +411,19 @@ def main():
             for dst, src in zip(h_outs, outs):
                 dst.copy_(src, non_blocking=True)
 
-    # Plain bf16 forward: the step's batch goes through in pieces, so the
-    # copy-in of one piece, the kernels of another and the copy-out of a third
-    # overlap (one stream each).  Every piece is an ordinary attn_fwd call on
-    # contiguous slices; the bytes copied per step are the same as above.
-    pipelined = not bwd and not fp8 and splits == 1
-    if pipelined:
-        pieces = e2e_chunks(B, H)
-        m_outs = {c: (torch.empty_like(o), torch.empty_like(lse)) for c in modes}
-        h_m_outs = {c: (torch.empty(o.shape, dtype=o.dtype).pin_memory(),
-                        torch.empty(lse.shape, dtype=lse.dtype).pin_memory()) for c in modes}
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-
-    def e2e_step_pipelined(main):
-        begin = torch.cuda.Event()
-        begin.record(main)
-        s_in.wait_event(begin)  # the previous step's kernels have read the inputs
-        for (b0, nb, h0, nh) in pieces:
-            sl = (slice(b0, b0 + nb), slice(h0, h0 + nh))
-            with torch.cuda.stream(s_in):
-                for dst, src in zip(ins, h_ins):
-                    dst[sl].copy_(src[sl], non_blocking=True)
-                arrived = torch.cuda.Event()
-                arrived.record(s_in)
-            main.wait_event(arrived)
-            kv_piece = kvl[b0:b0 + nb] if kvl is not None else None
-            for causal in modes:
-                oo, ll = m_outs[causal]
-                attn.attn_fwd(q[sl], k[sl], v[sl], oo[sl], ll[sl], nb, nh, S, S_kv, D, scale, causal, kv_piece,
-                              main)
-            computed = torch.cuda.Event()
-            computed.record(main)
-            s_out.wait_event(computed)
-            with torch.cuda.stream(s_out):
-                for causal in modes:
-                    for dst, src in zip(h_m_outs[causal], m_outs[causal]):
-                        dst[sl].copy_(src[sl], non_blocking=True)
-        copied = torch.cuda.Event()
-        copied.record(s_out)
-        main.wait_event(copied)  # the step ends when its last result is on the host
-
-    # The pipelined step is a few dozen launches and copies; it is captured
-    # once as a CUDA graph (the same attn_fwd calls and pinned copies) and
-    # replayed, so host-side launch overhead does not set the pace.
-    e2e_mode = "serial"
-    e2e_step = e2e_step_serial
-    if pipelined:
-        e2e_step_pipelined(stream)  # eager once: warms every piece's launch
-        torch.cuda.synchronize(dev)
-        try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                e2e_step_pipelined(torch.cuda.current_stream(dev))
-            torch.cuda.synchronize(dev)
-            e2e_step = graph.replay
-            e2e_mode = f"{len(pieces)} pieces, copy-in / kernels / copy-out overlapped, one CUDA graph per step"
-        except RuntimeError as exc:  # capture unsupported here: the serial step still measures end to end
-            torch.cuda.synchronize(dev)
-            e2e_mode = f"serial (graph capture failed: {str(exc).splitlines()[0][:120]})"
+    # Plain bf16 forward: the library's host-buffer executor (HostForward):
+    # the step's batch goes through in pieces whose copy-in, kernels and
+    # copy-out overlap on three streams, captured once as a CUDA graph.  The
+    # bytes copied per step are those of the serial step above.
+    e2e_mode, e2e_step = "serial", e2e_step_serial
+    if not bwd and not fp8 and splits == 1:
+        hf = attn.HostForward(B, H, S, S_kv, D, modes=modes, scale=scale, kv_valid_len=kvl, device=dev)
+        for dst, src in zip(hf.host_inputs, h_ins[:3]):
+            dst.copy_(src)
+        assert hf.h2d_bytes == h2d and hf.d2h_bytes == d2h
+        e2e_step = hf.run
+        e2e_mode = (f"HostForward: {len(hf.pieces)} pieces, copy-in / kernels / copy-out overlapped, "
+                    f"one CUDA graph per step")
 
     for _ in range(args.warmup):
         for causal in modes:

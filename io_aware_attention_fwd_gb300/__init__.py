@@ -1,7 +1,9 @@
 """Fused scaled-dot-product attention forward for GB300 (sm_103a).
 
 ``attn_fwd`` and friends mirror the C ABI of ``include/attn_fwd.h``;
-``attention_forward`` is a tensor-level convenience wrapper.  The CUDA
+``attention_forward`` is a tensor-level convenience wrapper, and
+``HostForward`` runs the forward pass on pinned host buffers with the copies
+overlapped.  The CUDA
 library is loaded on first use and must have been built (``build_ext``).
 """
 from ._lib import (ATTN_ERR_ALIGNMENT, ATTN_ERR_DEVICE, ATTN_ERR_INVALID_ARG, ATTN_ERR_LAUNCH,
@@ -13,6 +15,7 @@ from ._lib import (ATTN_ERR_ALIGNMENT, ATTN_ERR_DEVICE, ATTN_ERR_INVALID_ARG, AT
                    STATIC_SCRATCH_BYTES, attn_merge, attn_status_str, attn_watchdog_selftest, call_status,
                    load)
 from .api import attention_backward, attention_forward
+from .host import HostForward, plan_pieces
 from .build_ext import LIB_PATH, build
 
 __all__ = [
@@ -25,5 +28,5 @@ __all__ = [
     "attn_status_str",
     "attn_fwd_debug_status",
     "attn_watchdog_selftest", "attn_fwd_abi_version", "attention_forward", "load", "build",
-    "LIB_PATH",
+    "LIB_PATH", "HostForward", "plan_pieces",
 ]

@@ -167,25 +167,28 @@ def test_deterministic(dev):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("B,H,causal", [(4, 16, True), (1, 32, False), (2, 8, False)])
-def test_pieces_equal_one_launch(dev, B, H, causal):
-    # the benchmark's end-to-end leg runs a step as attn_fwd calls on
-    # contiguous pieces of the batch; each row's result must not depend on it
+@pytest.mark.parametrize("B,H,graph", [(4, 16, True), (1, 32, True), (2, 8, False)])
+def test_host_forward_equals_one_launch(dev, B, H, graph):
+    # HostForward runs a step as attn_fwd calls on contiguous pieces of the
+    # batch, with pinned copies on side streams (captured as a CUDA graph or
+    # eager): each row's O and LSE must equal one launch over the whole batch
     import torch
-    import bench
     import io_aware_attention_fwd_gb300 as attn
     S, D = 640, 64 if B == 4 else 128
     q, k, v = (parity.to_device(x, dev) for x in qkv(900 + B, B, H, S, S, D))
-    kvl = torch.tensor([640, 333][:B] + [640] * max(0, B - 2), dtype=torch.int32, device=dev) if B == 2 else None
-    o1, l1 = torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev)
-    attn.attn_fwd(q, k, v, o1, l1, B, H, S, S, D, 0.1, causal, kvl)
-    o2, l2 = torch.full_like(q, float("nan")), torch.full((B, H, S), float("nan"), device=dev)
-    for b0, nb, h0, nh in bench.e2e_chunks(B, H):
-        sl = (slice(b0, b0 + nb), slice(h0, h0 + nh))
-        attn.attn_fwd(q[sl], k[sl], v[sl], o2[sl], l2[sl], nb, nh, S, S, D, 0.1, causal,
-                      kvl[b0:b0 + nb] if kvl is not None else None)
+    kvl = torch.tensor([640, 333], dtype=torch.int32, device=dev) if B == 2 else None
+    hf = attn.HostForward(B, H, S, S, D, modes=(False, True), scale=0.1, kv_valid_len=kvl, device=dev, graph=graph)
+    for dst, src in zip(hf.host_inputs, (q, k, v)):
+        dst.copy_(src.cpu())
+    for _ in range(2):  # a replay reuses every buffer
+        hf.run()
     torch.cuda.synchronize()
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for causal in (False, True):
+        o1, l1 = torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev)
+        attn.attn_fwd(q, k, v, o1, l1, B, H, S, S, D, 0.1, causal, kvl)
+        torch.cuda.synchronize()
+        ho, hl = hf.host_outputs[causal]
+        assert torch.equal(o1.cpu(), ho) and torch.equal(l1.cpu(), hl)
 
 
 def test_side_stream_and_api_wrapper(dev):

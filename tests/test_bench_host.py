@@ -49,8 +49,9 @@ def _worker(rank, world, port, out):
 def test_e2e_pieces_cover_the_grid_once_contiguously(B, H):
     # the end-to-end leg moves each piece with one copy per tensor and runs it
     # as one attn_fwd call: whole batches, or a head range of one batch
+    from io_aware_attention_fwd_gb300.host import plan_pieces
     seen = set()
-    pieces = bench.e2e_chunks(B, H)
+    pieces = plan_pieces(B, H)
     for b0, nb, h0, nh in pieces:
         assert nb >= 1 and nh >= 1
         assert nb == 1 or (h0 == 0 and nh == H)
