@@ -132,8 +132,13 @@ struct BwdWork {
 
 __device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
   BwdWork w;
-  w.bh = static_cast<int>(blockIdx.x) / p.n_kv_tiles;
-  w.k0 = (static_cast<int>(blockIdx.x) % p.n_kv_tiles) * kBN;
+  if (p.causal) {  // key tile j walks n - j query tiles: every head's j = 0 first (longest first)
+    w.bh = static_cast<int>(blockIdx.x) % p.BH;
+    w.k0 = (static_cast<int>(blockIdx.x) / p.BH) * kBN;
+  } else {  // equal work: a head's key tiles side by side, sharing its Q and dO through L2
+    w.bh = static_cast<int>(blockIdx.x) / p.n_kv_tiles;
+    w.k0 = (static_cast<int>(blockIdx.x) % p.n_kv_tiles) * kBN;
+  }
   int nk = p.S_kv;
   if (p.kv_valid != nullptr) nk = min(max(__ldg(p.kv_valid + w.bh / p.H), 0), nk);
   w.nk_pad = nk;
