@@ -790,13 +790,25 @@ __global__ void __launch_bounds__(256) attn_bwd_prep(const uint16_t* __restrict_
     const int q = static_cast<int>(row % S_pad);
     float acc = 0.f, l2 = INFINITY;
     if (q < S_q) {
+      // each lane: kPer consecutive bf16 of O and dO in one 4- or 8-byte load,
+      // and the same kPer fp32 of the accumulator zeroed in one store
       const int64_t e0 = (bh * S_q + q) * D + lane * kPer;
+      uint32_t ow[kPer / 2], gw[kPer / 2];
+      if constexpr (kPer == 4) {
+        const uint2 a = __ldg(reinterpret_cast<const uint2*>(o + e0));
+        const uint2 g = __ldg(reinterpret_cast<const uint2*>(d_o + e0));
+        ow[0] = a.x; ow[kPer / 2 - 1] = a.y;
+        gw[0] = g.x; gw[kPer / 2 - 1] = g.y;
+        *reinterpret_cast<float4*>(dq_acc + e0) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        ow[0] = __ldg(reinterpret_cast<const uint32_t*>(o + e0));
+        gw[0] = __ldg(reinterpret_cast<const uint32_t*>(d_o + e0));
+        *reinterpret_cast<float2*>(dq_acc + e0) = make_float2(0.f, 0.f);
+      }
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) {
-        const float a = __uint_as_float(static_cast<uint32_t>(__ldg(o + e0 + e)) << 16);
-        const float b = __uint_as_float(static_cast<uint32_t>(__ldg(d_o + e0 + e)) << 16);
-        acc = fmaf(a, b, acc);
-        dq_acc[e0 + e] = 0.f;
+      for (int e = 0; e < kPer / 2; ++e) {
+        acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(gw[e] << 16), acc);
+        acc = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(gw[e] & 0xFFFF0000u), acc);
       }
       const float l = __ldg(lse + bh * S_q + q);
       l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
