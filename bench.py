@@ -411,24 +411,12 @@ def main():
             for dst, src in zip(h_outs, outs):
                 dst.copy_(src, non_blocking=True)
 
-    # Plain bf16 forward: the library's host-buffer executor (HostForward):
-    # the step's batch goes through in pieces whose copy-in, kernels and
-    # copy-out overlap on three streams, captured once as a CUDA graph.  The
-    # bytes copied per step are those of the serial step above.
-    e2e_mode, e2e_step = "serial", e2e_step_serial
-    if not bwd and not fp8 and splits == 1:
-        hf = attn.HostForward(B, H, S, S_kv, D, modes=modes, scale=scale, kv_valid_len=kvl, device=dev)
-        for dst, src in zip(hf.host_inputs, h_ins[:3]):
-            dst.copy_(src)
-        assert hf.h2d_bytes == h2d and hf.d2h_bytes == d2h
-        e2e_step = hf.run
-        e2e_mode = (f"HostForward: {len(hf.pieces)} pieces, copy-in / kernels / copy-out overlapped, "
-                    f"one CUDA graph per step")
-
+    # Device leg first (warm-up, then the timed steps), the end-to-end leg
+    # after it, so that a profiler counting launches finds the timed kernels
+    # right after the W x modes warm-up launches.
     for _ in range(args.warmup):
         for causal in modes:
             launch(causal)
-        e2e_step()
     torch.cuda.synchronize(dev)
     st = attn.attn_fwd_debug_status(stream)
     if st != attn.ATTN_OK:
@@ -460,9 +448,26 @@ def main():
     step_ms = [ev[i][0].elapsed_time(ev[i][n_l]) for i in range(args.steps)]
     launch_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(n_l)]
 
+    # End-to-end leg.  Plain bf16 forward: the library's host-buffer executor
+    # (HostForward): the step's batch goes through in pieces whose copy-in,
+    # kernels and copy-out overlap on three streams, captured once as a CUDA
+    # graph.  The bytes copied per step are those of the serial step above.
+    e2e_mode, e2e_step = "serial", e2e_step_serial
+    if not bwd and not fp8 and splits == 1:
+        hf = attn.HostForward(B, H, S, S_kv, D, modes=modes, scale=scale, kv_valid_len=kvl, device=dev)
+        for dst, src in zip(hf.host_inputs, h_ins[:3]):
+            dst.copy_(src)
+        assert hf.h2d_bytes == h2d and hf.d2h_bytes == d2h
+        e2e_step = hf.run
+        e2e_mode = (f"HostForward: {len(hf.pieces)} pieces, copy-in / kernels / copy-out overlapped, "
+                    f"one CUDA graph per step")
+    for _ in range(args.warmup):
+        e2e_step()
     e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(args.steps)]
     torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
     for i in range(args.steps):
         flush.zero_()
         e_ev[i][0].record(stream)

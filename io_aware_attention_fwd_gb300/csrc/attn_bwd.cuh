@@ -124,6 +124,8 @@ struct BwdSmem {
   __device__ uint32_t stage_free_h(int h) const { return h ? bar(23) : stage_free(); }
 };
 
+constexpr int kBwdHeadGroup = 16;  // causal launch order: heads per longest-first group
+
 // What one CTA covers: key tile j of head bh against query tiles
 // [i0, i0 + n).  Causal: only query tiles holding a query >= the first key.
 struct BwdWork {
@@ -132,9 +134,17 @@ struct BwdWork {
 
 __device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
   BwdWork w;
-  if (p.causal) {  // key tile j walks n - j query tiles: every head's j = 0 first (longest first)
-    w.bh = static_cast<int>(blockIdx.x) % p.BH;
-    w.k0 = (static_cast<int>(blockIdx.x) / p.BH) * kBN;
+  if (p.causal) {
+    // Key tile j walks n - j query tiles.  Heads go in groups of kBwdHeadGroup;
+    // inside a group the CTAs run longest first (every head's j = 0, then
+    // j = 1, ...), so the short CTAs fill the end, while only a group's fp32
+    // dQ accumulators are being reduced into at a time and stay in L2.
+    const int b = static_cast<int>(blockIdx.x);
+    const int g0 = b / (kBwdHeadGroup * p.n_kv_tiles) * kBwdHeadGroup;  // first head of the group
+    const int gs = min(kBwdHeadGroup, p.BH - g0);                        // heads in the group
+    const int idx = b - g0 * p.n_kv_tiles;
+    w.bh = g0 + idx % gs;
+    w.k0 = (idx / gs) * kBN;
   } else {  // equal work: a head's key tiles side by side, sharing its Q and dO through L2
     w.bh = static_cast<int>(blockIdx.x) / p.n_kv_tiles;
     w.k0 = (static_cast<int>(blockIdx.x) % p.n_kv_tiles) * kBN;
