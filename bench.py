@@ -14,7 +14,11 @@ softmax, lazy correction and the epilogue.
                    step, summed over ranks / max time over ranks.
   e2e              the same metric through the C ABI with host buffers:
                    pinned host -> device copies of Q, K, V and device -> host
-                   copies of O and LSE inside the timed region.
+                   copies of O and LSE inside the timed region.  Plain bf16
+                   forward workloads run it through HostForward (pieces of
+                   the batch with copy-in, kernels and copy-out overlapped,
+                   one CUDA graph per step); the others copy, compute and
+                   copy back in turn.  It runs after the device-timed steps.
   roofline         for the attention kernel (the only kernel in a step):
                    achieved = algorithmic FLOPs per launch / mean launch time,
                    against the measured dense bf16 peak.
