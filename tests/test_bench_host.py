@@ -63,6 +63,37 @@ def test_e2e_pieces_cover_the_grid_once_contiguously(B, H):
     assert len(pieces) <= max(4, B * 2)
 
 
+def test_profiled_traffic_needs_the_current_kernel_source(tmp_path, monkeypatch):
+    # a profile summary supplies the roofline's DRAM traffic only while its
+    # kernel-source hash matches the sources the bench runs
+    current = bench.kernel_source_hash()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "x.md").write_text(f"# x\n\nbench_workload: wl_a\nkernel_source_sha256_16: {current}\n"
+                               "dram_bytes_per_launch: 12345\n")
+    (prof / "y.md").write_text("# y\n\nbench_workload: wl_b\nkernel_source_sha256_16: 0000000000000000\n"
+                               "dram_bytes_per_launch: 999\n")
+    monkeypatch.setattr(bench, "ROOT", tmp_path)  # the lookup reads tmp_path/profiles
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: current)
+    assert bench.profiled_traffic("wl_a") == 12345.0
+    assert bench.profiled_traffic("wl_b") is None       # stale hash
+    assert bench.profiled_traffic("wl_c") is None       # no summary
+
+
+def test_committed_profiles_name_bench_workloads():
+    # every committed summary names a workload the bench knows and carries
+    # the three fields the lookup reads
+    import re
+    files = sorted((Path(bench.__file__).resolve().parent / "profiles").glob("*.md"))
+    assert files
+    for f in files:
+        text = f.read_text()
+        w = re.search(r"^bench_workload:\s*(\S+)", text, re.M)
+        assert w and w.group(1) in bench.WORKLOADS, f.name
+        assert re.search(r"^kernel_source_sha256_16:\s*[0-9a-f]{16}$", text, re.M), f.name
+        assert re.search(r"^dram_bytes_per_launch:\s*[0-9]+$", text, re.M), f.name
+
+
 def test_rank_aggregation_gloo_world2():
     import torch.multiprocessing as mp
     ctx = mp.get_context("spawn")
