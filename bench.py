@@ -6,7 +6,9 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 Prints ONE JSON line (rank 0).  A step is one forward pass of the workload in
 every mode it lists (e.g. non-causal and causal), i.e. the whole kernel path:
 tile schedule, TMA loads, QK^T and PV on the tensor cores, masking, online
-softmax, lazy correction and the epilogue.
+softmax, lazy correction and the epilogue.  The default workload is the
+long-context shape B=1, H=32, S=32768, D=128 (Q and K x2), causal and
+non-causal.
 
   value            algorithmic TFLOP/s (4 * D * allowed query-key pairs per
                    mode) with inputs resident in HBM, CUDA-event timed on the
@@ -24,6 +26,10 @@ softmax, lazy correction and the epilogue.
                    against the measured dense bf16 peak.
   cpu_baseline     the fp64 CPU oracle on a bounded sample of the same
                    workload, timed on the host cores (rank 0, N = 1 only).
+  per_config       the other plain forward shapes (4k worked example, 8k
+                   padded, 1k D=64), each timed in the same process with the
+                   same method (device leg only), per mode with its fraction
+                   of the peak.
 
 With N > 1 (torchrun) every rank runs its own replica (the path has no
 exchange step): scaling is weak.  --impl reference times the oracle instead
@@ -78,7 +84,12 @@ WORKLOADS = {
     "b4_h16_s1024_d64_bwd": dict(B=4, H=16, S=1024, D=64, modes=(False, True), seed=2, pass_="bwd"),
     "b1_h32_s8192_d128_bwd": dict(B=1, H=32, S=8192, D=128, modes=(True, False), seed=8, pass_="bwd"),
 }
-DEFAULT_WORKLOAD = "b4_h16_s1024_d64"
+# The headline: the long-context shape (32k tokens, 32 heads, D = 128), causal and
+# non-causal, the largest single-GPU configuration of the metric's s = 1k-32k range.
+DEFAULT_WORKLOAD = "b1_h32_s32768_d128_qkx2"
+# Timed in the same process after the headline (device leg only): the worked
+# example (4k), the padded 8k pair of sequences and the 1k, D = 64 batch.
+PER_CONFIG = ("b1_h32_s4096_d128", "b2_h32_s8192_d128_padded", "b4_h16_s1024_d64")
 
 
 def allowed_pairs(B, H, S_q, S_kv, causal, valid=None):
@@ -112,6 +123,23 @@ def alg_bytes(w, causal):
     B, H, S, D = w["B"], w["H"], w["S"], w["D"]
     kv = sum(min(w["valid"][b], s_kv(w)) if w.get("valid") else s_kv(w) for b in range(B))
     return H * (2 * S * D * 2 * B + 2 * kv * D * 2 + S * 4 * B)
+
+
+def workload_config(name, w, world):
+    """The ``config`` object of the JSON line; both arms print the same one."""
+    D = w["D"]
+    S_kv = s_kv(w)
+    eb = 1 if w.get("dtype") == "e4m3" else 2
+    big = w["B"] * w["H"] * (w["S"] + 2 * S_kv) * D * eb > 129e6  # Q + K + V against the 129 MB L2
+    return {"workload": name, "B": w["B"], "H": w["H"], "S_q": w["S"], "S_kv": S_kv, "D": D,
+            "kv_splits": w.get("splits", 1), "scale": 1.0 / math.sqrt(D),
+            "modes": ["causal" if c else "non-causal" for c in w["modes"]],
+            "kv_valid_len": list(w["valid"]) if w.get("valid") else None,
+            "q_mult": w.get("q_mult", 1.0), "k_mult": w.get("k_mult", 1.0),
+            "dtype": w.get("dtype", "bf16"), "pass": w.get("pass_", "fwd"),
+            "l2": ("inputs larger than L2, and L2 flushed before every timed step (256 MiB device write)" if big
+                   else "flushed before every timed step (256 MiB device write)"),
+            "parallelism": f"replicas x{world}"}
 
 
 def aggregate_ranks(flops_step, t_step_ms, t_e2e_ms, dist=None, device="cpu"):
@@ -226,6 +254,49 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(busy)}
 
 
+def time_plain_forward(attn, si, name, dev, stream, flush, steps, warmup):
+    """Device leg of a plain bf16 forward workload in this process: inputs
+    drawn on the device, ``warmup`` untimed steps, then ``steps`` steps each
+    after an L2 flush, every launch between CUDA events on its stream.
+    Returns the ``per_config`` entry (per mode: mean ms, TFLOP/s, fraction of
+    the peak)."""
+    import torch
+
+    w = WORKLOADS[name]
+    B, H, S, D = w["B"], w["H"], w["S"], w["D"]
+    S_kv = s_kv(w)
+    scale = 1.0 / math.sqrt(D)
+    q, k, v = si.qkv_bf16_torch(w["seed"], B, H, S, S_kv, D, w.get("q_mult", 1.0), w.get("k_mult", 1.0),
+                                device=dev)
+    o = torch.empty((B, H, S, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    kvl = torch.tensor(w["valid"], dtype=torch.int32, device=dev) if w.get("valid") else None
+    modes = w["modes"]
+    for _ in range(warmup):
+        for causal in modes:
+            attn.attn_fwd(q, k, v, o, lse, B, H, S, S_kv, D, scale, causal, kvl, stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(modes) + 1)] for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, causal in enumerate(modes):
+            attn.attn_fwd(q, k, v, o, lse, B, H, S, S_kv, D, scale, causal, kvl, stream)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    st = attn.attn_fwd_debug_status(stream)
+    if st != attn.ATTN_OK:
+        raise RuntimeError(f"device status after {name}: {attn.attn_status_str(st)}")
+    peak, _ = load_peaks()
+    out = {"config": workload_config(name, w, 1), "steps": steps, "warmup": warmup, "per_mode": {}}
+    for j, causal in enumerate(modes):
+        ms = sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
+        tf = alg_flops(w, causal) / (ms * 1e-3) / 1e12
+        out["per_mode"]["causal" if causal else "non-causal"] = {"ms": ms, "tflops": tf, "frac_of_peak": tf / peak}
+    del q, k, v, o, lse
+    return out
+
+
 def oracle_sample(w, q_bits, k_bits, v_bits, target_s, modes):
     """Time the fp64 oracle on a bounded row sample of the workload.
 
@@ -302,8 +373,7 @@ def run_reference(args, w, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 inputs)",
-        "config": {"workload": args.workload, **{k_: w[k_] for k_ in ("B", "H", "S", "D")},
-                   "modes": ["causal" if c else "non-causal" for c in w["modes"]]},
+        "config": workload_config(args.workload, w, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample, "cpu": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -321,6 +391,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-settle", action="store_true",
                     help="skip the 1 s busy loop before timing (for profiler runs)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config block (the other forward shapes, timed after the headline)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target oracle time for the cpu_baseline sample (0 disables)")
     args = ap.parse_args()
@@ -478,8 +550,13 @@ def main():
         e2e_step()
         e_ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    clocks = sampler.stop()
     e2e_ms = [a.elapsed_time(b) for a, b in e_ev]
+    per_config = {}
+    if not args.no_per_config:
+        for name in PER_CONFIG:
+            if name != args.workload:
+                per_config[name] = time_plain_forward(attn, si, name, dev, stream, flush, args.steps, args.warmup)
+    clocks = sampler.stop()
     st = attn.attn_fwd_debug_status(stream)
     if st != attn.ATTN_OK:
         raise RuntimeError(f"device status after timing: {attn.attn_status_str(st)}")
@@ -505,13 +582,7 @@ def main():
         "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
         "data": ("synthetic (seeded N(0,1) x16 rounded to e4m3 on the device, descale 1/16)" if fp8 else
                  "synthetic (seeded N(0,1) bf16 Q/K/V drawn on the device)"),
-        "config": {"workload": args.workload, "B": B, "H": H, "S_q": S, "S_kv": S_kv, "D": D,
-                   "kv_splits": splits,
-                   "scale": scale, "modes": ["causal" if c else "non-causal" for c in modes],
-                   "kv_valid_len": list(w["valid"]) if w.get("valid") else None,
-                   "q_mult": w.get("q_mult", 1.0), "k_mult": w.get("k_mult", 1.0),
-                   "l2": "flushed before every timed step (256 MiB device write)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(args.workload, w, world),
         "per_mode": per_mode,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
@@ -525,6 +596,8 @@ def main():
         "gpu_launches": args.steps * n_l * kernels_per_call,
         "clocks": clocks,
     }
+    if per_config:
+        line["per_config"] = per_config
 
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         import numpy as np

@@ -15,8 +15,12 @@
  *   - Same page, section "FlashAttention", and the "Flash attention" glossary
  *     page (news.hamidun.com), second paragraph: the output is built block by
  *     block over the keys and values with running softmax statistics, so the
- *     s x s matrix is never written to HBM.  This library allocates nothing;
- *     its working set is on-chip (shared memory and tensor memory).
+ *     s x s matrix is never written to HBM.  The forward calls allocate
+ *     nothing; their working set is on-chip (shared memory and tensor
+ *     memory).  The library's device image does carry one fixed array of
+ *     ATTN_STATIC_SCRATCH_BYTES (32 MiB), the scratch of
+ *     attn_fwd_splitkv_static, which every device that loads the library
+ *     holds until the process exits.
  *   - "PyTorch attention backends" story (hyper.ai), masked_fill sentences:
  *     a masked key is filled with -inf before the softmax.  Key j is allowed
  *     for row i iff j < S_kv, j < kv_valid_len[b] (when given) and, if causal,
@@ -188,9 +192,11 @@ attn_status_t attn_merge(const float* o_parts, const float* lse_parts, int n_par
  * more than ATTN_STATIC_SCRATCH_BYTES (use fewer splits, or attn_fwd_splitkv
  * with your own workspace).
  *
- * The first call on each device looks up the array's device address with
- * that device current (cudaGetSymbolAddress) and keeps it; make that first
- * call before any stream capture begins.
+ * The first call on each device that splits the keys (n_splits > 1, S_q > 0
+ * and S_kv > 0) looks up the array's device address with that device current
+ * (cudaGetSymbolAddress) and keeps it; make that first call before any
+ * stream capture begins.  Calls that do not split go straight to attn_fwd
+ * and never touch the array.
  *
  * The array is shared by every call in the process and keeps whatever the
  * last call left in it; nothing needs to start at zero, because each call

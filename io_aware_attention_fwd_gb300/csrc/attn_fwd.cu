@@ -1468,6 +1468,10 @@ attn_status_t attn_fwd_splitkv_static(const void* q, const void* k, const void* 
   const int64_t rows = static_cast<int64_t>(B) * H * S_q;
   if (n_splits > 1 && splitkv_workspace_bytes(rows, D, n_splits) > ATTN_STATIC_SCRATCH_BYTES)
     return ATTN_ERR_UNSUPPORTED;  // the partials would not fit in the fixed scratch
+  // Without a split (or with nothing to compute) the scratch is never used:
+  // the unsplit path runs without looking up its address.
+  if (n_splits == 1 || S_q == 0 || S_kv == 0)
+    return attn_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, causal, kv_valid_len, stream);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_DEVICE;
   const attn_status_t ps = prepare_device(dev);

@@ -121,7 +121,8 @@ def test_single_rank_aggregation():
 def test_reference_arm_under_torchrun_world2():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), str(ROOT / "bench.py"),
-           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-seconds", "0.3"]
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-seconds", "0.3",
+           "--workload", "b4_h16_s1024_d64"]
     res = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert res.returncode == 0, res.stderr[-2000:]
     lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
@@ -129,4 +130,18 @@ def test_reference_arm_under_torchrun_world2():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
-    assert d["config"]["workload"] == bench.DEFAULT_WORKLOAD
+    # the same config object the GPU arm prints for this workload
+    assert d["config"] == bench.workload_config("b4_h16_s1024_d64", bench.WORKLOADS["b4_h16_s1024_d64"], 2)
+
+
+def test_default_workload_is_the_long_context_target():
+    # the headline runs the 32k, D = 128 shape in both modes; the other
+    # forward shapes are timed beside it
+    w = bench.WORKLOADS[bench.DEFAULT_WORKLOAD]
+    assert (w["B"], w["H"], w["S"], w["D"]) == (1, 32, 32768, 128)
+    assert set(w["modes"]) == {True, False}
+    assert all(n in bench.WORKLOADS and n != bench.DEFAULT_WORKLOAD for n in bench.PER_CONFIG)
+    cfg = bench.workload_config(bench.DEFAULT_WORKLOAD, w, 1)
+    assert cfg["l2"].startswith("inputs larger than L2")
+    assert bench.workload_config("b4_h16_s1024_d64", bench.WORKLOADS["b4_h16_s1024_d64"], 1)["l2"].startswith(
+        "flushed")

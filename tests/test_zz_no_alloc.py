@@ -14,28 +14,47 @@ import math
 import numpy as np
 import pytest
 
+import oracle
 import seeded_inputs as si
 from tests import parity
 
 
+_REFUSALS = r"""
+import re, sys
+from pathlib import Path
+import io_aware_attention_fwd_gb300 as attn
+header = (Path(sys.argv[1]) / "include" / "attn_fwd.h").read_text()
+m = re.search(r"#define ATTN_STATIC_SCRATCH_BYTES \((\d+)ull << (\d+)\)", header)
+assert m and int(m.group(1)) << int(m.group(2)) == attn.STATIC_SCRATCH_BYTES
+fake = 0x10000
+# 64 splits x 8 heads x 4096 rows x 129 floats is over 32 MiB: refused before any launch
+need = attn.attn_fwd_splitkv_workspace_bytes(1, 8, 4096, 128, 64)
+assert need > attn.STATIC_SCRATCH_BYTES
+st = attn.call_status(attn.attn_fwd_splitkv_static, fake, fake, fake, fake, fake, 1, 8, 4096, 4096,
+                      128, 0.1, False, None, 64)
+assert st == attn.ATTN_ERR_UNSUPPORTED, st
+st = attn.call_status(attn.attn_fwd_splitkv_static, fake, fake, fake, fake, fake, 1, 8, 4096, 4096,
+                      128, 0.1, False, None, 0)
+assert st == attn.ATTN_ERR_INVALID_ARG, st
+print("refusals ok")
+"""
+
+
 def test_static_entry_rejects_sizes_beyond_the_fixed_scratch():
-    import re
+    # The refusals are checked in a child process that sees no CUDA device:
+    # the fake pointers below could never reach a kernel, and a refusal that
+    # came only after a device call would show up as ATTN_ERR_DEVICE instead.
+    import os
+    import subprocess
+    import sys
     from pathlib import Path
     import io_aware_attention_fwd_gb300 as attn
     attn.build()
-    header = (Path(__file__).resolve().parent.parent / "include" / "attn_fwd.h").read_text()
-    m = re.search(r"#define ATTN_STATIC_SCRATCH_BYTES \((\d+)ull << (\d+)\)", header)
-    assert m and int(m.group(1)) << int(m.group(2)) == attn.STATIC_SCRATCH_BYTES
-    fake = 0x10000
-    # 64 splits x 8 heads x 4096 rows x 129 floats is over 32 MiB: refused before any launch
-    need = attn.attn_fwd_splitkv_workspace_bytes(1, 8, 4096, 128, 64)
-    assert need > attn.STATIC_SCRATCH_BYTES
-    st = attn.call_status(attn.attn_fwd_splitkv_static, fake, fake, fake, fake, fake, 1, 8, 4096, 4096,
-                          128, 0.1, False, None, 64)
-    assert st == attn.ATTN_ERR_UNSUPPORTED
-    st = attn.call_status(attn.attn_fwd_splitkv_static, fake, fake, fake, fake, fake, 1, 8, 4096, 4096,
-                          128, 0.1, False, None, 0)
-    assert st == attn.ATTN_ERR_INVALID_ARG
+    root = Path(__file__).resolve().parent.parent
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", PYTHONPATH=str(root))
+    res = subprocess.run([sys.executable, "-c", _REFUSALS, str(root)], capture_output=True, text=True,
+                         timeout=300, env=env, cwd=root)
+    assert res.returncode == 0 and "refusals ok" in res.stdout, res.stderr[-2000:]
 
 
 @pytest.mark.gpu
@@ -72,3 +91,7 @@ def test_static_entry_matches_workspace_entry_twice():
         o_a, l_a = parity.gather_rows(o, lse)
         o_b, l_b = parity.gather_rows(o_ref, l_ref)
         parity.compare(o_a, l_a, o_b, l_b)
+        # and both against the fp64 oracle on the same inputs
+        o_or, l_or = oracle.attention_f64(q, k, v, scale, causal, kv_valid_len=valid)
+        parity.compare(o_a, l_a, o_or, l_or)
+        parity.compare(o_b, l_b, o_or, l_or)
