@@ -13,7 +13,12 @@ non-causal.
   value            algorithmic TFLOP/s (4 * D * allowed query-key pairs per
                    mode) with inputs resident in HBM, CUDA-event timed on the
                    launching stream, L2 flushed (256 MiB write) before every
-                   step, summed over ranks / max time over ranks.
+                   step, summed over ranks / max time over ranks.  Events sit
+                   only at the ends of a step: the launches inside it run
+                   back to back, each allowed to start its prologue while the
+                   previous one finishes (programmatic dependent launch).
+  per_mode         each mode's launch timed alone (flush, event, launch,
+                   event), so its own launch latency is included.
   e2e              the same metric through the C ABI with host buffers:
                    pinned host -> device copies of Q, K, V and device -> host
                    copies of O and LSE inside the timed region.  Plain bf16
@@ -22,14 +27,15 @@ non-causal.
                    one CUDA graph per step); the others copy, compute and
                    copy back in turn.  It runs after the device-timed steps.
   roofline         for the attention kernel (the only kernel in a step):
-                   achieved = algorithmic FLOPs per launch / mean launch time,
+                   achieved = algorithmic FLOPs per launch / mean launch time
+                   over the timed steps (step time / launches per step),
                    against the measured dense bf16 peak.
   cpu_baseline     the fp64 CPU oracle on a bounded sample of the same
                    workload, timed on the host cores (rank 0, N = 1 only).
   per_config       the other plain forward shapes (4k worked example, 8k
                    padded, 1k D=64), each timed in the same process with the
-                   same method (device leg only), per mode with its fraction
-                   of the peak.
+                   same method (device leg only: step value and per mode),
+                   with fractions of the peak.
 
 With N > 1 (torchrun) every rank runs its own replica (the path has no
 exchange step): scaling is weak.  --impl reference times the oracle instead
@@ -254,6 +260,49 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(busy)}
 
 
+def time_steps(launch, modes, steps, flush, stream):
+    """Step times (ms): L2 flush, then one launch per mode back to back, with
+    CUDA events only at the step's two ends, so consecutive launches keep
+    their programmatic overlap (an event between them would end it)."""
+    import torch
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        for causal in modes:
+            launch(causal)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def time_modes(launch, modes, steps, flush, stream):
+    """Per-mode launch times (ms): each mode alone between two events after
+    an L2 flush, ``steps`` times."""
+    import torch
+
+    out = {}
+    for causal in modes:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            launch(causal)
+            b.record(stream)
+        torch.cuda.synchronize()
+        out[causal] = sum(a.elapsed_time(b) for a, b in ev) / steps
+    return out
+
+
+def per_mode_entry(w, mode_ms, peak):
+    return {("causal" if c else "non-causal"): {
+        "ms": ms, "tflops": alg_flops(w, c) / (ms * 1e-3) / 1e12,
+        "frac_of_peak": alg_flops(w, c) / (ms * 1e-3) / 1e12 / peak} for c, ms in mode_ms.items()}
+
+
 def time_plain_forward(attn, si, name, dev, stream, flush, steps, warmup):
     """Device leg of a plain bf16 forward workload in this process: inputs
     drawn on the device, ``warmup`` untimed steps, then ``steps`` steps each
@@ -272,27 +321,24 @@ def time_plain_forward(attn, si, name, dev, stream, flush, steps, warmup):
     lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
     kvl = torch.tensor(w["valid"], dtype=torch.int32, device=dev) if w.get("valid") else None
     modes = w["modes"]
+
+    def launch(causal):
+        attn.attn_fwd(q, k, v, o, lse, B, H, S, S_kv, D, scale, causal, kvl, stream)
+
     for _ in range(warmup):
         for causal in modes:
-            attn.attn_fwd(q, k, v, o, lse, B, H, S, S_kv, D, scale, causal, kvl, stream)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(modes) + 1)] for _ in range(steps)]
-    torch.cuda.synchronize(dev)
-    for i in range(steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        for j, causal in enumerate(modes):
-            attn.attn_fwd(q, k, v, o, lse, B, H, S, S_kv, D, scale, causal, kvl, stream)
-            ev[i][j + 1].record(stream)
-    torch.cuda.synchronize(dev)
+            launch(causal)
+    step_ms = time_steps(launch, modes, steps, flush, stream)
+    mode_ms = time_modes(launch, modes, steps, flush, stream)
     st = attn.attn_fwd_debug_status(stream)
     if st != attn.ATTN_OK:
         raise RuntimeError(f"device status after {name}: {attn.attn_status_str(st)}")
     peak, _ = load_peaks()
-    out = {"config": workload_config(name, w, 1), "steps": steps, "warmup": warmup, "per_mode": {}}
-    for j, causal in enumerate(modes):
-        ms = sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
-        tf = alg_flops(w, causal) / (ms * 1e-3) / 1e12
-        out["per_mode"]["causal" if causal else "non-causal"] = {"ms": ms, "tflops": tf, "frac_of_peak": tf / peak}
+    t = sum(step_ms) / len(step_ms)
+    tf = sum(alg_flops(w, c) for c in modes) / (t * 1e-3) / 1e12
+    out = {"config": workload_config(name, w, 1), "steps": steps, "warmup": warmup,
+           "ms_per_step": t, "tflops": tf, "frac_of_peak": tf / peak,
+           "per_mode": per_mode_entry(w, mode_ms, peak)}
     del q, k, v, o, lse
     return out
 
@@ -508,21 +554,14 @@ def main():
         torch.cuda.synchronize(dev)
 
     n_l = len(modes)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_l + 1)] for _ in range(args.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        for j, causal in enumerate(modes):
-            launch(causal)
-            ev[i][j + 1].record(stream)
-    torch.cuda.synchronize(dev)
+    step_ms = time_steps(launch, modes, args.steps, flush, stream)
     if dist is not None:
         dist.barrier()
-    step_ms = [ev[i][0].elapsed_time(ev[i][n_l]) for i in range(args.steps)]
-    launch_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(n_l)]
+    # each mode alone (its own launch latency exposed), after the timed steps
+    mode_ms = time_modes(launch, modes, args.steps, flush, stream)
 
     # End-to-end leg.  Plain bf16 forward: the library's host-buffer executor
     # (HostForward): the step's batch goes through in pieces whose copy-in,
@@ -565,16 +604,14 @@ def main():
     value, e2e_value, t_step, t_e2e = aggregate_ranks(
         flops_step, sum(step_ms) / len(step_ms), sum(e2e_ms) / len(e2e_ms), dist, dev)
 
-    # roofline of the attention kernel: every launch in the step is attn_fwd_sm103a<D>
-    mean_launch_ms = sum(sum(x) for x in launch_ms) / (args.steps * n_l)
+    # Roofline of the attention kernel: every launch in the step is the same
+    # kernel (one per mode), so its mean launch duration over the timed region
+    # is the step time over the launches per step.
+    mean_launch_ms = sum(step_ms) / (args.steps * n_l)
     flops_launch = flops_step / n_l
     peak, peak_src = load_peaks(w.get("dtype", "bf16"))
     achieved = flops_launch / (mean_launch_ms * 1e-3) / 1e12
-    per_mode = {("causal" if c else "non-causal"): {
-        "ms": sum(launch_ms[j]) / args.steps,
-        "tflops": alg_flops(w, c) / (sum(launch_ms[j]) / args.steps * 1e-3) / 1e12,
-        "frac_of_peak": alg_flops(w, c) / (sum(launch_ms[j]) / args.steps * 1e-3) / 1e12 / peak,
-    } for j, c in enumerate(modes)}
+    per_mode = per_mode_entry(w, mode_ms, peak)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

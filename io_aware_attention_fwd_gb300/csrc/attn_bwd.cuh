@@ -713,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_u32(smem_raw);
   if ((base & 1023u) != 0u) {  // the layout has no slack for realignment: report, run nothing
+    grid_dependency_wait();     // still complete only after the kernel before, like every launch here
     if (threadIdx.x == 0) atomicOr(&g_attn_status, 2u);
     return;
   }
@@ -721,7 +722,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
-  const BwdWork wk = bwd_work(p);
 
   if (threadIdx.x == 0) {
     mbar_init(sm.kv_full(), 1);
@@ -759,6 +759,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const WaitCtx w{p.timeout_ns, misc + 1};
+  // On-chip set-up is done; global memory (the statistics and the zeroed dQ
+  // accumulator of the kernel before, kv_valid_len) is read from here on.
+  grid_dependency_wait();
+  const BwdWork wk = bwd_work(p);
 
   if (warp == 0) {
     if (lane == 0 && wk.n > 0) bwd_load_role<D>(sm, &tmQ, &tmK, &tmV, &tmDO, wk, w);
@@ -773,6 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bwd_dq_role<D>(sm, &tmDQ, tmem, p, wk, w);
     }
   }
+  grid_launch_dependents();  // this thread has issued all of its work
 
   tc_fence_before();
   __syncthreads();
@@ -792,6 +797,8 @@ __global__ void __launch_bounds__(256) attn_bwd_prep(const uint16_t* __restrict_
                                                      float* __restrict__ delta, float* __restrict__ dq_acc, int S_q,
                                                      int S_pad, int64_t BH) {
   constexpr int kPer = D / 32;
+  grid_dependency_wait();  // O and LSE come from the forward pass
+  grid_launch_dependents();
   const int lane = static_cast<int>(threadIdx.x & 31);
   const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t step = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -835,6 +842,8 @@ __global__ void __launch_bounds__(256) attn_bwd_prep(const uint16_t* __restrict_
 // dQ = bf16(scale * accumulator), four elements per thread step.
 __global__ void __launch_bounds__(256) attn_bwd_dq_convert(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq,
                                                            int64_t n4, float scale) {
+  grid_dependency_wait();  // the accumulator is complete once the gradient kernel is
+  grid_launch_dependents();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 a = __ldg(reinterpret_cast<const float4*>(dq_acc) + i);

@@ -215,6 +215,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// Programmatic dependent launch.  The kernel is launched so that it may start
+// while the previous kernel in its stream is still finishing: it builds its
+// on-chip state (barriers, tensor memory) first and waits here before its
+// first global memory access, until that kernel has completed and its writes
+// are visible.  Without the launch attribute the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream (if launched the same way) start its own
+// prologue on SMs this grid has left; its data accesses still wait for this
+// grid to complete.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --- tcgen05 ---------------------------------------------------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -559,9 +572,6 @@ template <int D, bool kF8>
 __device__ void load_role(const Smem<D, kF8>& sm, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                           const CUtensorMap* tmV, const Params& p, const WaitCtx& w) {
   using C = Cfg<D, kF8>;
-  tma_prefetch_desc(tmQ);
-  tma_prefetch_desc(tmK);
-  tma_prefetch_desc(tmV);
   const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
   const int rounds = (p.n_units + G - 1) / G;
   int it = 0;  // K/V items issued
@@ -599,6 +609,7 @@ __device__ void load_role(const Smem<D, kF8>& sm, const CUtensorMap* tmQ, const 
       }
     }
   }
+  grid_launch_dependents();  // every load of this CTA is issued
   // Every issued copy must land before the CTA can exit (one shared deadline).
   bool drained = (k == 0) || mbar_wait_drain(sm.bar_q(), (k - 1) & 1, w);
   for (int i = (it > C::kSlots ? it - C::kSlots : 0); i < it && drained; ++i)
@@ -921,6 +932,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sm.bar_turn(), kBM);
     misc[1] = 0u;
     fence_barrier_init();
+  } else if (threadIdx.x == 32) {
+    tma_prefetch_desc(&tmQ);  // the tensor maps are kernel parameters, not
+    tma_prefetch_desc(&tmK);  // data of the previous kernel
+    tma_prefetch_desc(&tmV);
   }
   if (warp == 1) {
     tmem_alloc(base + C::kMiscOff, kTmemCols);
@@ -931,6 +946,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const WaitCtx w{p.timeout_ns, misc + 1};
+  // Everything above is on-chip; from here on the kernel reads the previous
+  // kernel's outputs (Q, K, V, kv_valid_len) and writes O and LSE.
+  grid_dependency_wait();
 
   if (warp == 0) {
     if (lane == 0) load_role<D, kF8>(sm, &tmQ, &tmK, &tmV, p, w);
@@ -939,6 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     softmax_role<D, kSplit, kF8>(sm, (warp - 4) >> 2, tmem, p, w);
   }
+  grid_launch_dependents();  // this thread has issued all of its work
 
   tc_fence_before();
   __syncthreads();
@@ -951,6 +970,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // S_kv == 0: every row has no allowed key -> O = 0, LSE = -inf.
 __global__ void attn_fill_empty(uint16_t* o, float* lse, int64_t rows, int D) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     for (int d = 0; d < D; ++d) o[i * D + d] = 0;
@@ -977,6 +998,8 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
   constexpr int kPer = D / 32;  // 4 (float4 per lane) or 2 (float2)
   constexpr int kBatch = 8;     // partial rows in flight per warp
   using Vec = typename std::conditional<kPer == 4, float4, float2>::type;
+  grid_dependency_wait();  // the partials come from the kernel before
+  grid_launch_dependents();
   const int lane = static_cast<int>(threadIdx.x & 31);
   const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t step = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -1087,6 +1110,26 @@ bool encode_3d(CUtensorMap* m, const void* ptr, int D, int S, int64_t BH, int eb
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Every kernel of the library is launched with programmatic dependent launch:
+// it may begin while the previous kernel in the stream is finishing, and
+// waits (griddepcontrol.wait) before its first global memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, 2 unsupported
 std::atomic<int> g_dev_sms[kMaxDevices];
@@ -1159,26 +1202,27 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   prm.o_scale = o_scale;
   prm.o_part = o_part;
   prm.lse_part = lse_part;
-  const int grid = std::min(prm.n_units, sms);  // persistent: at most one CTA per SM
+  const dim3 grid(static_cast<unsigned>(std::min(prm.n_units, sms)));  // persistent: at most one CTA per SM
+  cudaError_t e;
   if constexpr (kF8)
-    attn_fwd_sm103a<D, false, true><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    e = launch_pdl(attn_fwd_sm103a<D, false, true>, grid, dim3(kThreads), C::kSmemBytes, stream, tq, tk, tv, prm);
   else if (n_splits > 1)
-    attn_fwd_sm103a<D, true, false><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
+    e = launch_pdl(attn_fwd_sm103a<D, true, false>, grid, dim3(kThreads), C::kSmemBytes, stream, tq, tk, tv, prm);
   else
-    attn_fwd_sm103a<D, false, false><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, prm);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    e = launch_pdl(attn_fwd_sm103a<D, false, false>, grid, dim3(kThreads), C::kSmemBytes, stream, tq, tk, tv, prm);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 attn_status_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t rows, int D, void* o,
                            float* lse, int sms, cudaStream_t stream) {
-  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 16);
-  if (D == 64)
-    attn_merge_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_parts, lse_parts, n_parts, rows, rows,
-                                                                            static_cast<uint16_t*>(o), lse);
-  else
-    attn_merge_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_parts, lse_parts, n_parts, rows, rows,
-                                                                             static_cast<uint16_t*>(o), lse);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  const dim3 blocks(static_cast<unsigned>(std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 16)));
+  uint16_t* o16 = static_cast<uint16_t*>(o);
+  const cudaError_t e =
+      D == 64 ? launch_pdl(attn_merge_kernel<64>, blocks, dim3(256), 0, stream, o_parts, lse_parts, n_parts, rows, rows,
+                           o16, lse)
+              : launch_pdl(attn_merge_kernel<128>, blocks, dim3(256), 0, stream, o_parts, lse_parts, n_parts, rows, rows,
+                           o16, lse);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 // Argument checks shared by attn_fwd and attn_fwd_splitkv (nothing is launched).
@@ -1217,10 +1261,10 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   float* lse2 = static_cast<float*>(workspace);
   float* delta = lse2 + BH * S_pad;
   float* dq_acc = delta + BH * S_pad;
-  const int64_t prep_blocks = std::min<int64_t>((BH * S_pad + 7) / 8, static_cast<int64_t>(sms) * 16);
-  attn_bwd_prep<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_o), lse, lse2, delta, dq_acc, S_q, S_pad, BH);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  const dim3 prep_blocks(static_cast<unsigned>(std::min<int64_t>((BH * S_pad + 7) / 8, static_cast<int64_t>(sms) * 16)));
+  if (launch_pdl(attn_bwd_prep<D>, prep_blocks, dim3(256), 0, stream, static_cast<const uint16_t*>(o),
+                 static_cast<const uint16_t*>(d_o), lse, lse2, delta, dq_acc, S_q, S_pad, BH) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!encode_3d(&tq, q, D, S_q, BH) || !encode_3d(&tk, k, D, S_kv, BH) || !encode_3d(&tv, v, D, S_kv, BH) ||
       !encode_3d(&tdo, d_o, D, S_q, BH) || !encode_3d(&tdq, dq_acc, D, S_q, BH, 4))
@@ -1243,14 +1287,16 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   prm.scale = scale;
   prm.causal = causal;
   prm.timeout_ns = kDefaultTimeoutNs;
-  const int64_t grid = BH * prm.n_kv_tiles;
-  attn_bwd_sm103a<D><<<static_cast<unsigned>(grid), kThreads, BwdCfg<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  const dim3 grid(static_cast<unsigned>(BH * prm.n_kv_tiles));
+  if (launch_pdl(attn_bwd_sm103a<D>, grid, dim3(kThreads), BwdCfg<D>::kSmemBytes, stream, tq, tk, tv, tdo, tdq,
+                 prm) != cudaSuccess)
+    return ATTN_ERR_LAUNCH;
   const int64_t n4 = BH * S_q * D / 4;
-  const int64_t cv_blocks = std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(sms) * 16);
-  attn_bwd_dq_convert<<<static_cast<unsigned>(cv_blocks), 256, 0, stream>>>(dq_acc, static_cast<uint16_t*>(dq), n4,
-                                                                            scale);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  const dim3 cv_blocks(static_cast<unsigned>(std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(sms) * 16)));
+  return launch_pdl(attn_bwd_dq_convert, cv_blocks, dim3(256), 0, stream, static_cast<const float*>(dq_acc),
+                    static_cast<uint16_t*>(dq), n4, scale) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_LAUNCH;
 }
 
 constexpr int kMaxSplits = 64;
@@ -1316,9 +1362,10 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 
   if (S_kv == 0) {
     const int64_t rows = BH * S_q;
-    const int64_t blocks = std::min<int64_t>((rows + 255) / 256, 4096);
-    attn_fill_empty<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<uint16_t*>(o), lse, rows, D);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    const dim3 blocks(static_cast<unsigned>(std::min<int64_t>((rows + 255) / 256, 4096)));
+    return launch_pdl(attn_fill_empty, blocks, dim3(256), 0, st, static_cast<uint16_t*>(o), lse, rows, D) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_LAUNCH;
   }
   if (!get_encoder()) return ATTN_ERR_DEVICE;
   const int sms = g_dev_sms[dev].load(std::memory_order_relaxed);
@@ -1346,9 +1393,10 @@ attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (S_kv == 0) {
     const int64_t rows = static_cast<int64_t>(B) * H * S_q;
-    const int64_t blocks = std::min<int64_t>((rows + 255) / 256, 4096);
-    attn_fill_empty<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<uint16_t*>(o), lse, rows, D);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+    const dim3 blocks(static_cast<unsigned>(std::min<int64_t>((rows + 255) / 256, 4096)));
+    return launch_pdl(attn_fill_empty, blocks, dim3(256), 0, st, static_cast<uint16_t*>(o), lse, rows, D) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_LAUNCH;
   }
   if (!get_encoder()) return ATTN_ERR_DEVICE;
   return launch<128, true>(q, k, v, o, lse, B, H, S_q, S_kv, static_cast<float>(s_all), causal, kv_valid_len,

@@ -21,6 +21,21 @@ import math
 from . import _lib
 
 
+# Piece-count rule, from pinned-copy bandwidth measured against copy size on
+# GB300 (NVLink-C2C host link): one copy reaches about 90% of the ~205 GB/s
+# host-to-device plateau from 4 MiB up, while 1-2 MiB copies run at 45-100
+# GB/s; and beyond 4 pieces the per-piece kernel tails cost more than the
+# shorter exposed first copy-in and last copy-out save.
+MIN_PIECE_BYTES = 4 << 20
+MAX_PIECES = 4
+
+
+def auto_pieces(q_bytes: int) -> int:
+    """Pieces for a step whose Q tensor has ``q_bytes``: as many as keep each
+    piece's Q copy at MIN_PIECE_BYTES or more, at most MAX_PIECES."""
+    return max(1, min(MAX_PIECES, int(q_bytes) // MIN_PIECE_BYTES))
+
+
 def plan_pieces(B: int, H: int, target: int = 4):
     """About ``target`` pieces (b0, nb, h0, nh) of the [B][H] grid, each either
     whole batches (h0 = 0, nh = H) or a head range of one batch (nb = 1), so
@@ -41,8 +56,9 @@ class HostForward:
     B, H, S_q, S_kv, D: shapes as for ``attn_fwd``.  modes: the mask modes run
     per step (False = non-causal, True = causal), each with its own outputs.
     kv_valid_len: int32 CUDA tensor [B] or None, fixed for the executor's
-    life.  pieces: target number of pieces.  graph: capture the step as a
-    CUDA graph (else every ``run`` issues the launches and copies eagerly).
+    life.  pieces: target number of pieces (None: ``auto_pieces`` of the Q
+    tensor's size).  graph: capture the step as a CUDA graph (else every
+    ``run`` issues the launches and copies eagerly).
 
     Fill ``host_inputs`` (q, k, v: pinned bf16 [B,H,S,D]) before ``run()``;
     after the stream has reached the end of a step, ``host_outputs[mode]``
@@ -50,7 +66,7 @@ class HostForward:
     """
 
     def __init__(self, B: int, H: int, S_q: int, S_kv: int, D: int, modes=(False,),
-                 scale: float | None = None, kv_valid_len=None, device="cuda", pieces: int = 4,
+                 scale: float | None = None, kv_valid_len=None, device="cuda", pieces: int | None = None,
                  graph: bool = True):
         import torch
 
@@ -61,6 +77,8 @@ class HostForward:
         self.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
         self.device = torch.device(device)
         self.kv_valid_len = kv_valid_len
+        if pieces is None:
+            pieces = auto_pieces(B * H * S_q * D * 2)
         self.pieces = plan_pieces(B, H, pieces)
         bf = torch.bfloat16
         dev = self.device

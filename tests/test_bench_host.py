@@ -63,6 +63,17 @@ def test_e2e_pieces_cover_the_grid_once_contiguously(B, H):
     assert len(pieces) <= max(4, B * 2)
 
 
+def test_auto_piece_count_follows_the_copy_size_rule():
+    # each piece's Q copy stays at 4 MiB or more, with at most 4 pieces
+    from io_aware_attention_fwd_gb300.host import MAX_PIECES, MIN_PIECE_BYTES, auto_pieces
+    assert auto_pieces(1) == 1 and auto_pieces(MIN_PIECE_BYTES - 1) == 1
+    assert auto_pieces(4 * 16 * 1024 * 64 * 2) == 2        # 1k, D=64 batch: 8 MiB of Q
+    assert auto_pieces(32 * 4096 * 128 * 2) == MAX_PIECES  # 4k worked example: 32 MiB of Q
+    assert auto_pieces(32 * 32768 * 128 * 2) == MAX_PIECES
+    for n in range(MIN_PIECE_BYTES, 64 * MIN_PIECE_BYTES, MIN_PIECE_BYTES // 3):
+        assert n // auto_pieces(n) >= MIN_PIECE_BYTES
+
+
 def test_profiled_traffic_needs_the_current_kernel_source(tmp_path, monkeypatch):
     # a profile summary supplies the roofline's DRAM traffic only while its
     # kernel-source hash matches the sources the bench runs
