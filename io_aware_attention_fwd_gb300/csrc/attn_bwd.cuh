@@ -166,12 +166,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
-__device__ __forceinline__ void st_shared_v4_b32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // One key row of P^T for kN query columns of a tile: p = 2^(c s - lse2),
 // packed to bf16 pairs.  kMask: column col is allowed iff col >= first.
@@ -228,20 +222,20 @@ __device__ void bwd_load_role(const BwdSmem<D>& sm, const CUtensorMap* tmQ, cons
   for (int t = 0; t < wk.n; ++t) {
     const int y = (wk.i0 + t) * kBM;
     const int qs = t % C::kQSlots;
-    if (t >= C::kQSlots && !mbar_wait(sm.q_empty(qs), ((t / C::kQSlots) - 1) & 1, w)) break;
+    if (t >= C::kQSlots && !bwd_wait(sm.q_empty(qs), ((t / C::kQSlots) - 1) & 1, w)) break;
     mbar_expect_tx(sm.q_full(qs), C::kTileBytes);
     for (int pn = 0; pn < C::kPanels; ++pn) tma_load_3d(sm.q(qs) + pn * kPanelBytes, tmQ, sm.q_full(qs), pn * 64, y, wk.bh);
     ++nq;
-    if (t > 0 && !mbar_wait(sm.do_empty(), (t - 1) & 1, w)) break;
+    if (t > 0 && !bwd_wait(sm.do_empty(), (t - 1) & 1, w)) break;
     mbar_expect_tx(sm.do_full(), C::kTileBytes);
     for (int pn = 0; pn < C::kPanels; ++pn) tma_load_3d(sm.d_o() + pn * kPanelBytes, tmDO, sm.do_full(), pn * 64, y, wk.bh);
     ++ndo;
   }
   // every issued copy lands before the CTA may exit (one shared deadline)
-  bool drained = mbar_wait_drain(sm.kv_full(), 0, w);
+  bool drained = bwd_wait_drain(sm.kv_full(), 0, w);
   for (int u = (nq > C::kQSlots ? nq - C::kQSlots : 0); u < nq && drained; ++u)
-    drained = mbar_wait_drain(sm.q_full(u % C::kQSlots), (u / C::kQSlots) & 1, w);
-  if (drained && ndo > 0) mbar_wait_drain(sm.do_full(), (ndo - 1) & 1, w);
+    drained = bwd_wait_drain(sm.q_full(u % C::kQSlots), (u / C::kQSlots) & 1, w);
+  if (drained && ndo > 0) bwd_wait_drain(sm.do_full(), (ndo - 1) & 1, w);
 }
 
 // MMA issuer: warp-wide control flow, one elected lane issues.
@@ -259,14 +253,14 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
   const uint64_t do_k = sdesc_kmajor_sw128(sm.d_o());
   const uint64_t do_mn = sdesc_mnmajor_sw128(sm.d_o(), kPanelBytes);
   const uint32_t tS = tmem + C::kSCol, tDP = tmem + C::kDPCol, tDV = tmem + C::kDVCol, tDK = tmem + C::kDKCol;
-  bool ok = __all_sync(0xffffffffu, mbar_wait(sm.kv_full(), 0, w) && mbar_wait(sm.q_full(0), 0, w));
+  bool ok = __all_sync(0xffffffffu, bwd_wait(sm.kv_full(), 0, w) && bwd_wait(sm.q_full(0), 0, w));
   bool issued = false;
   if (ok) {
     tc_fence_after();
     issue_qk<D, false>(leader, tS, kd, sdesc_kmajor_sw128(sm.q(0)), idesc_s);  // S^T_0 = K Q_0^T
     tc_commit_if(leader, sm.s_full());
     issued = true;
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.do_full(), 0, w));
+    ok = __all_sync(0xffffffffu, bwd_wait(sm.do_full(), 0, w));
   }
   if (ok) {
     tc_fence_after();
@@ -277,21 +271,21 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
     const int qs = t % C::kQSlots;
     const uint64_t q_mn = sdesc_mnmajor_sw128(sm.q(qs), kPanelBytes);
     // dV += P^T dO_t  (P^T read from TMEM before S^T_{t+1} overwrites it: in-order MMAs)
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.p_ready(), t & 1, w));
+    ok = __all_sync(0xffffffffu, bwd_wait(sm.p_ready(), t & 1, w));
     if (!ok) break;
     tc_fence_after();
     bwd_issue_ts<D>(leader, tDV, tS, do_mn, idesc_acc, t > 0);
     tc_commit_if(leader, sm.do_empty());
     if (t + 1 < wk.n) {  // S^T_{t+1}
       const int qn = (t + 1) % C::kQSlots;
-      ok = __all_sync(0xffffffffu, mbar_wait(sm.q_full(qn), ((t + 1) / C::kQSlots) & 1, w));
+      ok = __all_sync(0xffffffffu, bwd_wait(sm.q_full(qn), ((t + 1) / C::kQSlots) & 1, w));
       if (!ok) break;
       tc_fence_after();
       issue_qk<D, false>(leader, tS, kd, sdesc_kmajor_sw128(sm.q(qn)), idesc_s);
       tc_commit_if(leader, sm.s_full());
     }
     // dK += dS^T Q_t (dS^T from TMEM), then dQ_t = dS K into the dP^T columns
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.ds_ready(), t & 1, w));
+    ok = __all_sync(0xffffffffu, bwd_wait(sm.ds_ready(), t & 1, w));
     if (!ok) break;
     tc_fence_after();
     bwd_issue_ts<D>(leader, tDK, tDP, q_mn, idesc_acc, t > 0);
@@ -304,7 +298,7 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
     tc_commit_if(leader, sm.dsm_free());
     tc_commit_if(leader, sm.q_empty(qs));
     if (t + 1 < wk.n) {  // dP^T_{t+1}, once dQ_t has been read out of its columns
-      ok = __all_sync(0xffffffffu, mbar_wait(sm.do_full(), (t + 1) & 1, w) && mbar_wait(sm.dq_free(), t & 1, w));
+      ok = __all_sync(0xffffffffu, bwd_wait(sm.do_full(), (t + 1) & 1, w) && bwd_wait(sm.dq_free(), t & 1, w));
       if (!ok) break;
       tc_fence_after();
       issue_qk<D, false>(leader, tDP, vd, do_k, idesc_s);
@@ -314,7 +308,7 @@ __device__ void bwd_mma_role(const BwdSmem<D>& sm, uint32_t tmem, const BwdWork&
   if (issued) {
     tc_commit_if(leader, sm.done());
     tc_commit_if(leader, sm.drain());
-    __all_sync(0xffffffffu, mbar_wait_drain(sm.drain(), 0, w));
+    __all_sync(0xffffffffu, bwd_wait_drain(sm.drain(), 0, w));
   }
 }
 
@@ -352,11 +346,11 @@ __device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem,
       next_dl = __ldg(p.delta + srow0 + (t + 1) * kBM);
     }
     mbar_arrive(sm.stat(t & 1));
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.stat(t & 1), (t >> 1) & 1, w));
+    ok = __all_sync(0xffffffffu, bwd_wait(sm.stat(t & 1), (t >> 1) & 1, w));
     if (!ok) break;
 
     // P^T row: p_c = 2^(c*s_c - lse2_c) for the allowed (key, query) pairs
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.s_full(), t & 1, w));
+    ok = __all_sync(0xffffffffu, bwd_wait(sm.s_full(), t & 1, w));
     if (!ok) break;
     tc_fence_after();
     // Masking only on tiles that need it (the causal diagonal, or padded
@@ -386,8 +380,8 @@ __device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem,
     mbar_arrive(sm.p_ready());
 
     // dS^T row: p * (dP^T - delta), to TMEM (for dK) and shared memory (for dQ)
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.dp_full(), t & 1, w));
-    if (ok && t > 0) ok = __all_sync(0xffffffffu, mbar_wait(sm.dsm_free(), (t - 1) & 1, w));
+    ok = __all_sync(0xffffffffu, bwd_wait(sm.dp_full(), t & 1, w));
+    if (ok && t > 0) ok = __all_sync(0xffffffffu, bwd_wait(sm.dsm_free(), (t - 1) & 1, w));
     if (!ok) break;
     tc_fence_after();
 #pragma unroll
@@ -426,7 +420,7 @@ __device__ void bwd_row_role(const BwdSmem<D>& sm, uint8_t* smem, uint32_t tmem,
 
   // dK and dV rows out of TMEM (zero when the CTA had no work)
   bool have = ok && wk.n > 0;
-  if (have) have = __all_sync(0xffffffffu, mbar_wait(sm.done(), 0, w));
+  if (have) have = __all_sync(0xffffffffu, bwd_wait(sm.done(), 0, w));
   if (have) tc_fence_after();
 #pragma unroll 1
   for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (times scale)
@@ -466,9 +460,6 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t
       "r"(src), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Key rows with two warpgroups (D = 64): warpgroup hf takes query columns
 // [64 hf, 64 hf + 64) of every tile -- P^T and dS^T need no row-wide
@@ -504,7 +495,7 @@ __device__ void bwd_row_role2(const BwdSmem<D>& sm, uint8_t* smem, const CUtenso
   int nstaged = 0;
   // dQ of tile tt (this half's columns) out of TMEM, staged, and reduce-added
   auto reduce_dq = [&](int tt) -> bool {
-    if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), tt & 1, w))) return false;
+    if (!__all_sync(0xffffffffu, bwd_wait(sm.dq_full(), tt & 1, w))) return false;
     tc_fence_after();
     uint32_t a[32];
     tmem_ld32(tQ, a);
@@ -516,7 +507,7 @@ __device__ void bwd_row_role2(const BwdSmem<D>& sm, uint8_t* smem, const CUtenso
         bulk_wait_read_all();
         mbar_arrive(sm.stage_free_h(hf));
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(sm.stage_free_h(hf), (nstaged - 1) & 1, w))) return false;
+      if (!__all_sync(0xffffffffu, bwd_wait(sm.stage_free_h(hf), (nstaged - 1) & 1, w))) return false;
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -525,7 +516,7 @@ __device__ void bwd_row_role2(const BwdSmem<D>& sm, uint8_t* smem, const CUtenso
     fence_async_smem();
     mbar_arrive(sm.staged_h(hf));
     if (leader) {  // rows past the head's last query fall outside the tensor map and are skipped
-      if (!mbar_wait(sm.staged_h(hf), nstaged & 1, w)) return false;
+      if (!bwd_wait(sm.staged_h(hf), nstaged & 1, w)) return false;
       tma_reduce_add_3d(tmDQ, box, 32 * hf, (wk.i0 + tt) * kBM, wk.bh);
       bulk_commit();
       issued = true;
@@ -539,7 +530,7 @@ __device__ void bwd_row_role2(const BwdSmem<D>& sm, uint8_t* smem, const CUtenso
     st[(r < 64 ? 0 : 64) + (r & 63)] = next_v;
     if (t + 1 < wk.n) next_v = __ldg(src + srow0 + (t + 1) * kBM);
     mbar_arrive(sm.stat_h(hf, t & 1));
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.stat_h(hf, t & 1), (t >> 1) & 1, w));
+    ok = __all_sync(0xffffffffu, bwd_wait(sm.stat_h(hf, t & 1), (t >> 1) & 1, w));
     if (!ok) break;
     if (t > 0 && !reduce_dq(t - 1)) {
       ok = false;
@@ -547,7 +538,7 @@ __device__ void bwd_row_role2(const BwdSmem<D>& sm, uint8_t* smem, const CUtenso
     }
 
     // P^T row: p_c = 2^(c*s_c - lse2_c) for the allowed (key, query) pairs
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.s_full(), t & 1, w));
+    ok = __all_sync(0xffffffffu, bwd_wait(sm.s_full(), t & 1, w));
     if (!ok) break;
     tc_fence_after();
     uint32_t sr[kN];
@@ -569,8 +560,8 @@ __device__ void bwd_row_role2(const BwdSmem<D>& sm, uint8_t* smem, const CUtenso
     mbar_arrive(sm.p_ready());
 
     // dS^T row: p * (dP^T - delta), to TMEM (for dK) and shared memory (for dQ)
-    ok = __all_sync(0xffffffffu, mbar_wait(sm.dp_full(), t & 1, w));
-    if (ok && t > 0) ok = __all_sync(0xffffffffu, mbar_wait(sm.dsm_free(), (t - 1) & 1, w));
+    ok = __all_sync(0xffffffffu, bwd_wait(sm.dp_full(), t & 1, w));
+    if (ok && t > 0) ok = __all_sync(0xffffffffu, bwd_wait(sm.dsm_free(), (t - 1) & 1, w));
     if (!ok) break;
     tc_fence_after();
 #pragma unroll
@@ -611,7 +602,7 @@ __device__ void bwd_row_role2(const BwdSmem<D>& sm, uint8_t* smem, const CUtenso
 
   // this half's head-dim columns of the dK and dV rows (zero when the CTA had no work)
   bool have = ok && wk.n > 0;
-  if (have) have = __all_sync(0xffffffffu, mbar_wait(sm.done(), 0, w));
+  if (have) have = __all_sync(0xffffffffu, bwd_wait(sm.done(), 0, w));
   if (have) tc_fence_after();
 #pragma unroll 1
   for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (times scale)
@@ -653,7 +644,7 @@ __device__ void bwd_dq_role(const BwdSmem<D>& sm, const CUtensorMap* tmDQ, uint3
   bool issued = false;
   int nround = 0;  // staging rounds so far
   for (int t = 0; t < wk.n; ++t) {
-    if (!__all_sync(0xffffffffu, mbar_wait(sm.dq_full(), t & 1, w))) break;
+    if (!__all_sync(0xffffffffu, bwd_wait(sm.dq_full(), t & 1, w))) break;
     tc_fence_after();
     // read the whole row first and release its TMEM columns (the next dP^T
     // product waits for them)
@@ -673,7 +664,7 @@ __device__ void bwd_dq_role(const BwdSmem<D>& sm, const CUtensorMap* tmDQ, uint3
     bool ok = true;
 #pragma unroll
     for (int rd = 0; rd < kBoxes / 2; ++rd) {
-      ok = __all_sync(0xffffffffu, nround == 0 || mbar_wait(sm.stage_free(), (nround - 1) & 1, w));
+      ok = __all_sync(0xffffffffu, nround == 0 || bwd_wait(sm.stage_free(), (nround - 1) & 1, w));
       if (!ok) break;
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
@@ -687,7 +678,7 @@ __device__ void bwd_dq_role(const BwdSmem<D>& sm, const CUtensorMap* tmDQ, uint3
       fence_async_smem();
       mbar_arrive(sm.staged());
       if (leader) {  // rows past the head's last query fall outside the tensor map and are skipped
-        ok = mbar_wait(sm.staged(), nround & 1, w);
+        ok = bwd_wait(sm.staged(), nround & 1, w);
         if (ok) {
           tma_reduce_add_3d(tmDQ, sm.stage(), 64 * rd, q0, wk.bh);
           tma_reduce_add_3d(tmDQ, sm.stage() + kBoxBytes, 64 * rd + 32, q0, wk.bh);

@@ -22,21 +22,24 @@
 //
 // Persistent kernel: one CTA per SM walks a static list of work units.  A
 // unit is two 128-row query tiles of one (batch, head) against that head's
-// allowed keys.  Warp roles (384 threads):
+// allowed keys.  Warp roles (512 threads, four warpgroups):
 //   warp 0       TMA producer: per unit the two Q tiles, then K/V tiles into a
 //                ring of shared-memory slots guarded by mbarriers.  The ring
 //                runs on across units, so the next unit's Q and first K/V
 //                tiles load while the current unit finishes.
-//   warp 1       tcgen05.mma issuer (one thread): S_t = Q_t K_j^T into TMEM,
-//                then O_t += P_t V_j with P_t read from TMEM.
+//   warp 1       tcgen05.mma issuer (one elected lane): S_t = Q_t K_j^T into
+//                TMEM, then O_t += P_t V_j with P_t read from TMEM.
 //   warps 4-7    softmax for query tile 0; warps 8-11 for query tile 1.  One
 //                thread owns one query row (one TMEM lane): it reads its S
-//                row, masks, updates the running max and sum, writes P (bf16)
-//                back over S, rescales O lazily, and writes O and LSE at the
-//                end of the unit straight from registers to global memory.
+//                row, masks, updates the running max and sum, writes P
+//                (bf16) back over S, and rescales its O row in TMEM when the
+//                max grew by more than 2^8 (lazy correction).
+//   warps 12-15  epilogue: O / l rounded to bf16 and written with TMA tensor
+//                stores from shared memory, LSE with coalesced stores.
 // While one softmax warpgroup works on its tile, the tensor core runs the
 // other tile's MMAs, so exp2 work and MMAs overlap; across units, the next
-// unit's S MMAs run while the softmax warpgroups drain the previous O.
+// unit's first steps run while the epilogue warpgroup drains the previous
+// O.
 //
 // Every wait on a barrier is bounded by a %globaltimer deadline.  A wait that
 // gives up sets a shared abort flag and a device status word, and every role
@@ -63,7 +66,10 @@ constexpr int kBM = 128;              // query rows per softmax tile (TMEM lanes
 constexpr int kBN = 128;              // keys per kv tile
 constexpr int kQTiles = 2;            // query tiles per work unit
 constexpr int kRowsPerUnit = kBM * kQTiles;
-constexpr int kThreads = 384;         // warps 0-3: roles, 4-7 / 8-11: softmax
+constexpr int kThreads = 384;         // backward kernel: warps 0-3 roles, 4-11 key rows / dQ
+constexpr int kFwdThreads = 512;      // forward kernel: warps 0-3 roles, 4-7 / 8-11 softmax, 12-15 epilogue
+constexpr int kEpiWarp0 = 12;         // first warp of the forward kernel's epilogue warpgroup
+constexpr int kStagePanelBytes = 32 * 128;  // one epilogue warp's O staging: 32 rows x 64 bf16
 constexpr uint32_t kTmemCols = 512;   // S0 | S1 | O0 | O1
 constexpr int kPanelBytes = 128 * 128;   // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
@@ -84,16 +90,20 @@ struct Cfg {
   static constexpr int kKeysPerStep = 32 / kEB;       // keys per P.V MMA K step
   static constexpr int kPvSteps = kBN / kKeysPerStep;
   static constexpr int kPCols = kBN * kEB / 4;        // TMEM columns of packed P
+  static constexpr int kOPanels = D / 64;             // 128-byte (64 x bf16) panels of an O row
   // K/V ring depth.  At D = 64 a shallow ring measured best: all CTAs start
   // together and a deep ring makes them all ask DRAM for many tiles at once.
-  static constexpr int kSlots = kF8 ? 12 : ((D == 128) ? 5 : 4);
+  // At D = 128 four slots leave room for the O staging buffer.
+  static constexpr int kSlots = kF8 ? 10 : 4;
   static constexpr bool kTurn = !kF8 && D == 128;  // softmax warpgroups alternate
   static constexpr int kQOff = 0;
   static constexpr int kSlotOff = kQTiles * kTileBytes;
-  static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
+  static constexpr int kStageOff = kSlotOff + kSlots * kTileBytes;  // O staging, 4 KB per epilogue warp
+  static constexpr int kStatOff = kStageOff + 4 * kStagePanelBytes;  // float2 (m, l) [kQTiles][kBM]
+  static constexpr int kBarOff = kStatOff + kQTiles * kBM * 8;
   // barriers: q_full | q_free[2] | full[kSlots] | empty[kSlots] | s_full[2] | p_full[2] |
-  //           o_done[2] | drain | turn
-  static constexpr int kNumBars = 1 + kQTiles + 2 * kSlots + 3 * kQTiles + 2;
+  //           o_done[2] | drain | turn | o_free[2] | epi[2]
+  static constexpr int kNumBars = 1 + kQTiles + 2 * kSlots + 3 * kQTiles + 2 + 2 * kQTiles;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] tmem base, [1] abort flag
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024 B alignment
   static constexpr int kOCol0 = kQTiles * kBN;             // first O column in TMEM
@@ -178,7 +188,9 @@ struct WaitCtx {
 
 // Slow path of a bounded wait.  honour_abort=false is used while draining
 // work already in flight, which must finish even after another role gave up.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
+// Inlined: warpgroups with different register budgets (setmaxnreg) cannot
+// share one out-of-line function.
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
                                             volatile uint32_t* abort_flag, bool honour_abort) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -195,6 +207,42 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsig
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, w.timeout_ns, w.abort_flag, true);
+}
+
+// The backward kernel has one register budget for the whole CTA, so it keeps
+// the slow path out of line (smaller hot loops; measured 2-3% faster there).
+__device__ __noinline__ bool mbar_wait_slow_call(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
+                                                 volatile uint32_t* abort_flag, bool honour_abort) {
+  return mbar_wait_slow(bar, parity, timeout_ns, abort_flag, honour_abort);
+}
+__device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow_call(bar, parity, w.timeout_ns, w.abort_flag, true);
+}
+__device__ __forceinline__ bool bwd_wait_drain(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow_call(bar, parity, w.timeout_ns, w.abort_flag, false);
+}
+
+// A wait that is expected to last long (a whole work unit): between polls
+// the warp sleeps, 64 ns doubling up to 512 ns, so that idle warps leave
+// the SM's issue slots and power to the working ones.  Bounded like
+// mbar_wait.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t ns = 64;
+  while (!mbar_try_wait(bar, parity)) {
+    if (*w.abort_flag != 0u) return false;
+    if (globaltimer_ns() - t0 > w.timeout_ns) {
+      *w.abort_flag = 1u;
+      atomicOr(&g_attn_status, 1u);
+      return false;
+    }
+    __nanosleep(ns);
+    ns = ns < 512u ? 2u * ns : 512u;
+  }
+  return true;
 }
 
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const WaitCtx& w) {
@@ -227,6 +275,52 @@ __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepco
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// shared -> global tensor copy of one box (coordinates of its first element)
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of this thread's bulk copies have been read
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's bulk copies are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// generic-proxy shared-memory writes become visible to the async proxy (TMA)
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4_b32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Per-warpgroup register budgets of the forward kernel (all four warps of a
+// warpgroup execute the same one): the softmax warpgroups take registers the
+// others give back.  A launch of kFwdThreads gives every thread
+// kRegsAtLaunch; setmaxnreg.dec may only lower that and .inc only raise it
+// (anything else is an illegal instruction), so the checks are compile-time.
+constexpr uint32_t kRegsAtLaunch = 65536 / kFwdThreads;
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  static_assert(N >= 24 && N % 8 == 0 && N <= kRegsAtLaunch, "setmaxnreg.dec lowers the launch budget");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  static_assert(N <= 256 && N % 8 == 0 && N >= kRegsAtLaunch, "setmaxnreg.inc raises the launch budget");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Sets this warpgroup's budget to N: lowers or raises it as N requires.
+template <uint32_t N>
+__device__ __forceinline__ void regs_set() {
+  if constexpr (N < kRegsAtLaunch) regs_dec<N>();
+  if constexpr (N > kRegsAtLaunch) regs_inc<N>();
+}
+constexpr uint32_t kRegsRoles = 104;    // warps 0-3: TMA producer, MMA issuer (more measured faster)
+constexpr uint32_t kRegsSoftmax = 168;  // warps 4-11
+constexpr uint32_t kRegsEpi = 72;       // warps 12-15
+static_assert(kRegsRoles + 2 * kRegsSoftmax + kRegsEpi == 4 * kRegsAtLaunch,
+              "the budgets share out exactly the launch's registers");
 
 // --- tcgen05 ---------------------------------------------------------------
 
@@ -471,7 +565,10 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
 template <int D, bool kF8>
 struct Smem {
   uint32_t base;  // shared address, 1024-aligned
+  uint8_t* ptr;   // the same byte as a generic pointer
   __device__ uint32_t q(int t) const { return base + Cfg<D, kF8>::kQOff + t * Cfg<D, kF8>::kTileBytes; }
+  __device__ uint32_t stage(int qw) const { return base + Cfg<D, kF8>::kStageOff + qw * kStagePanelBytes; }
+  __device__ float2* stat(int t) const { return reinterpret_cast<float2*>(ptr + Cfg<D, kF8>::kStatOff) + t * kBM; }
   __device__ uint32_t slot(int s) const { return base + Cfg<D, kF8>::kSlotOff + s * Cfg<D, kF8>::kTileBytes; }
   __device__ uint32_t bar(int i) const { return base + Cfg<D, kF8>::kBarOff + 8 * i; }
   __device__ uint32_t bar_q() const { return bar(0); }
@@ -483,6 +580,9 @@ struct Smem {
   __device__ uint32_t bar_o(int t) const { return bar(1 + 3 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
   __device__ uint32_t bar_drain() const { return bar(1 + 4 * kQTiles + 2 * Cfg<D, kF8>::kSlots); }
   __device__ uint32_t bar_turn() const { return bar(2 + 4 * kQTiles + 2 * Cfg<D, kF8>::kSlots); }
+  // epilogue warpgroup hand-offs
+  __device__ uint32_t bar_ofree(int t) const { return bar(3 + 4 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
+  __device__ uint32_t bar_epi(int t) const { return bar(3 + 5 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
 };
 
 // One work unit: two 128-row query tiles of one (batch, head).
@@ -621,9 +721,9 @@ __device__ void load_role(const Smem<D, kF8>& sm, const CUtensorMap* tmQ, const 
 // commits.  Per unit and kv step j, for each query tile t that still has
 // keys: O_t (+)= P_t V_j, then S_t = Q_t K_{j+1}^T.  P_t is read before the
 // next S_t overwrites it because MMAs issued by one thread execute in order.
-// The first P_t V of a unit overwrites O_t only after P_t of that unit is
-// ready, which the softmax warps signal after they have read the previous
-// unit's O_t out of TMEM.
+// Each P_t V waits for P_t (softmax); the first of a unit also waits until
+// the epilogue warpgroup has read the previous unit's O_t out of TMEM
+// (o_free).
 template <int D, bool kF8>
 __device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p, const WaitCtx& w) {
   using C = Cfg<D, kF8>;
@@ -671,6 +771,7 @@ __device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p,
         if (!ok || j >= un.nkv[t]) continue;
         ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_p(t), pc[t] & 1, w));
         ++pc[t];
+        if (ok && j == 0 && k > 0) ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_ofree(t), (k - 1) & 1, w));
         if (!ok) continue;
         tc_fence_after();
         issue_pv<D, kF8>(leader, tO[t], tS[t], vd0 + sv * kSlotStep, idesc_pv, j > 0);
@@ -697,20 +798,25 @@ __device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p,
   }
 }
 
-// Softmax + epilogue for query tile t (128 threads, one query row each).
-// kSplit: the unit covers one key chunk and writes fp32 O and LSE partials.
+// Softmax for query tile t (128 threads, one query row each).  Per kv step it
+// reads its S row from TMEM, masks, updates the running max and sum, writes
+// P (bf16, or e4m3) back over S and, when the row max grew by more than 2^8,
+// rescales O in TMEM before releasing P (lazy correction).  At the end of a
+// unit it hands the row's statistics (m, l) to the epilogue warpgroup, which
+// normalises and stores O and LSE.
 template <int D, bool kSplit, bool kF8>
 __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const Params& p, const WaitCtx& w) {
   using C = Cfg<D, kF8>;
   const int r = static_cast<int>(threadIdx.x) - kBM * (1 + t);  // row in tile == TMEM lane
-  const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16;
+  const int qw = r >> 5;                                         // lane quarter (warp % 4)
+  const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
   const uint32_t tS = tmem + lane_off + t * kBN;
-  const uint32_t tO = tmem + lane_off + C::kOCol0 + t * D;
   const float c = p.scale_log2;
   const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
   const int rounds = (p.n_units + G - 1) / G;
   int cnt = 0;    // kv tiles this query tile has processed (S_full / O_done phases)
   int sbase = 0;  // softmax steps of both query tiles in this CTA's earlier units
+  int k = 0;      // units finished
   bool ok = true;
   for (int rr = 0; rr < rounds && ok; ++rr) {
     const int u = unit_of(rr, cta, G);
@@ -803,12 +909,14 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
       for (int cc = 0; cc < C::kPCols; cc += 32) tmem_st32(tS + cc, pk + cc);
       if (C::kTurn) mbar_arrive(sm.bar_turn());
       tmem_wait_st();
-
       // Lazy correction: O is rescaled only when some row's max grew by > 2^8.
+      // (Kept in the softmax warps: every hand-off to a separate warpgroup
+      // measured slower than this rarely taken branch.)
       if (__any_sync(0xffffffffu, rescale_o)) {
         ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (cnt + j - 1) & 1, w));
         if (ok) {
           tc_fence_after();
+          const uint32_t tO = tmem + lane_off + C::kOCol0 + t * D;
           const uint64_t a2 = pack_f32x2(alpha, alpha);
 #pragma unroll 1
           for (int cc = 0; cc < D; cc += 32) {
@@ -829,88 +937,157 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
       }
       tc_fence_before();
       mbar_arrive(sm.bar_p(t));
-      if (!ok) break;
     }
-
-    // Epilogue: read O out of TMEM in two halves (after the second, O_t is
-    // free for the next unit), scale by 1/l, round to bf16 and store the row
-    // with 16-byte stores; LSE is (m + log2 l) ln 2, one coalesced fp32 store
-    // per row.
-    bool have_o = ok;
-    if (have_o) have_o = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (cnt + nkv - 1) & 1, w));
     cnt += nkv;
     sbase += n0 + n1;
-    if (have_o) tc_fence_after();
-    float inv_l = 0.f, lse = -INFINITY;
-    if (l > 0.f) {
-      inv_l = p.o_scale / l;  // o_scale: the V descale of the e4m3 path, else 1
-      lse = (m_c + log2f(l)) * kLn2;
-    }
-    const int64_t grow = static_cast<int64_t>(un.bh) * p.S_q + row;
-    const int64_t prow = static_cast<int64_t>(un.split) * p.BH * p.S_q + grow;  // split mode
-    uint16_t* dst = p.o + grow * D;
-    const uint64_t il2 = pack_f32x2(inv_l, inv_l);
-    constexpr int kHalf = D / 2;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t o[kHalf];
-      if (have_o) {
-#pragma unroll
-        for (int cc = 0; cc < kHalf; cc += 32) tmem_ld32(tO + h * kHalf + cc, o + cc);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < kHalf; ++i) o[i] = 0u;
-      }
-      if (kSplit) {  // fp32 partial O of this key chunk (already divided by its own l)
-        if (row < p.S_q) {
-          float* pdst = p.o_part + prow * D + h * kHalf;
-#pragma unroll
-          for (int q = 0; q < kHalf / 4; ++q) {
-            float x[4];
-#pragma unroll
-            for (int e = 0; e < 4; e += 2)
-              unpack_f32x2(mul_f32x2(pack_f32x2(__uint_as_float(o[4 * q + e]), __uint_as_float(o[4 * q + e + 1])), il2),
-                           x[e], x[e + 1]);
-            st_global_v4(pdst + 4 * q, __float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
-                         __float_as_uint(x[3]));
-          }
-        }
-      } else if (row < p.S_q) {
-#pragma unroll
-        for (int q = 0; q < kHalf / 8; ++q) {
-          uint32_t wv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float x0, x1;
-            unpack_f32x2(
-                mul_f32x2(pack_f32x2(__uint_as_float(o[8 * q + 2 * e]), __uint_as_float(o[8 * q + 2 * e + 1])), il2),
-                x0, x1);
-            wv[e] = pack_bf16x2(x0, x1);
-          }
-          st_global_v4(dst + h * kHalf + 8 * q, wv[0], wv[1], wv[2], wv[3]);
-        }
-      }
-    }
-    if (row < p.S_q) {
-      if (kSplit)
-        p.lse_part[prow] = lse;
-      else
-        p.lse[grow] = lse;
-    }
+    if (!ok) break;
+    // End of the unit: the row statistics go to the epilogue warpgroup,
+    // once it has taken the previous unit's (that epilogue has also read the
+    // previous O_t out of TMEM).
+    if (k > 0) ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_ofree(t), (k - 1) & 1, w));
+    if (!ok) break;
+    sm.stat(t)[r] = make_float2(m_c, l);
+    mbar_arrive(sm.bar_epi(t));
+    ++k;
   }
 }
 
+// Epilogue warpgroup (warps 12-15): warp 12 + q serves TMEM lane quarter q
+// (rows 32q .. 32q + 31) of both query tiles.  At the end of each unit, tile
+// 0 then tile 1, it takes the softmax threads' row statistics (m, l), waits
+// for the tile's last P.V, reads O_t out of TMEM (which releases it for the
+// next unit's first P.V), scales it by 1/l, rounds to bf16 and writes it
+// through a 128-byte-swizzled shared-memory panel with TMA tensor stores
+// (one 32-row x 64-column box per panel; rows past S_q are clipped by the
+// tensor map).  LSE = (m + log2 l) ln 2 is one coalesced fp32 store per
+// row.  With key splitting it writes the fp32 partial O (divided by the
+// chunk's own l) and the chunk's LSE to the workspace instead.  Meanwhile
+// the softmax warps are already on the next unit's first steps.
 template <int D, bool kSplit, bool kF8>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ void epilogue_role(const Smem<D, kF8>& sm, const CUtensorMap* tmO, uint32_t tmem, const Params& p,
+                              const WaitCtx& w) {
+  using C = Cfg<D, kF8>;
+  const int qw = static_cast<int>(threadIdx.x >> 5) & 3;
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int rt = qw * 32 + lane;  // row within a query tile == TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+  const uint32_t stage = sm.stage(qw);
+  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  const int rounds = (p.n_units + G - 1) / G;
+  int cnt[kQTiles] = {0, 0};  // P.V products of each query tile in earlier units
+  int k = 0;                  // units finished
+  bool ok = true;
+  for (int rr = 0; rr < rounds && ok; ++rr) {
+    const int u = unit_of(rr, cta, G);
+    if (u >= p.n_units) continue;
+    const Unit un = make_unit(p, u);
+    // Epilogues of this unit's two query tiles.
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t) {
+      if (!ok) break;
+      const int nkv = un.nkv[t];
+      ok = __all_sync(0xffffffffu, mbar_wait_sleepy(sm.bar_epi(t), k & 1, w));
+      if (!ok) break;
+      const float2 ml = sm.stat(t)[rt];  // (m in scaled log2 units, l)
+      ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (cnt[t] + nkv - 1) & 1, w));
+      cnt[t] += nkv;
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tO = tmem + lane_off + C::kOCol0 + t * D;
+      const int row0 = un.q0 + t * kBM + qw * 32;  // this warp's first row
+      const int row = row0 + lane;
+      float inv_l = 0.f, lse = -INFINITY;
+      if (ml.y > 0.f) {
+        inv_l = p.o_scale / ml.y;  // o_scale: the V descale of the e4m3 path, else 1
+        lse = (ml.x + log2f(ml.y)) * kLn2;
+      }
+      const uint64_t il2 = pack_f32x2(inv_l, inv_l);
+      const int64_t grow = static_cast<int64_t>(un.bh) * p.S_q + row;
+      if constexpr (kSplit) {  // fp32 partial O of this key chunk, straight from registers
+        const int64_t prow = static_cast<int64_t>(un.split) * p.BH * p.S_q + grow;
+        float* pdst = p.o_part + prow * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc, o);
+          tmem_wait_ld();
+          if (row < p.S_q) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              float x[4];
+#pragma unroll
+              for (int e = 0; e < 4; e += 2)
+                unpack_f32x2(mul_f32x2(pack_f32x2(__uint_as_float(o[4 * q4 + e]), __uint_as_float(o[4 * q4 + e + 1])),
+                                       il2),
+                             x[e], x[e + 1]);
+              st_global_v4(pdst + cc + 4 * q4, __float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                           __float_as_uint(x[3]));
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(sm.bar_ofree(t));
+        if (row < p.S_q) p.lse_part[prow] = lse;
+      } else {
+        // Per 64-column panel: read it out of TMEM (after the last panel O_t
+        // is free for the next unit), scale, round to bf16, and write its 32
+        // rows x 128 B into the warp's staging panel in the 128-byte swizzle
+        // the tensor map expects (16-byte chunk c of row r at chunk position
+        // c ^ (r & 7)); then one TMA store.  The next panel is read out of
+        // TMEM while the previous store is still reading the staging panel.
+        const uint32_t rowa = stage + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+        for (int pn = 0; pn < C::kOPanels; ++pn) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t o[32];
+            tmem_ld32(tO + pn * 64 + h * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float x0, x1;
+              unpack_f32x2(mul_f32x2(pack_f32x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2), x0,
+                           x1);
+              pk[16 * h + i] = pack_bf16x2(x0, x1);
+            }
+          }
+          if (pn == C::kOPanels - 1) {
+            tc_fence_before();
+            mbar_arrive(sm.bar_ofree(t));
+          }
+          if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging panel
+          __syncwarp();
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4_b32(rowa + (static_cast<uint32_t>(ch ^ (lane & 7)) << 4), pk[4 * ch], pk[4 * ch + 1],
+                             pk[4 * ch + 2], pk[4 * ch + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (row0 < p.S_q) tma_store_3d(tmO, stage, pn * 64, row0, un.bh);
+            bulk_commit();
+          }
+        }
+        if (row < p.S_q) p.lse[grow] = lse;
+      }
+    }
+    ++k;
+  }
+  if (lane == 0) bulk_wait_all();  // every O store of this warp is complete before the CTA exits
+}
+
+template <int D, bool kSplit, bool kF8>
+__global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const Params p) {
   using C = Cfg<D, kF8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const Smem<D, kF8> sm{base};
+  const Smem<D, kF8> sm{base, smem};
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -927,6 +1104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sm.bar_s(t), 1);
       mbar_init(sm.bar_p(t), kBM);
       mbar_init(sm.bar_o(t), 1);
+      mbar_init(sm.bar_ofree(t), kBM);  // the four epilogue warps
+      mbar_init(sm.bar_epi(t), kBM);    // the tile's softmax threads
     }
     mbar_init(sm.bar_drain(), 1);
     mbar_init(sm.bar_turn(), kBM);
@@ -936,6 +1115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);  // the tensor maps are kernel parameters, not
     tma_prefetch_desc(&tmK);  // data of the previous kernel
     tma_prefetch_desc(&tmV);
+    if (!kSplit) tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(base + C::kMiscOff, kTmemCols);
@@ -950,12 +1130,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kernel's outputs (Q, K, V, kv_valid_len) and writes O and LSE.
   grid_dependency_wait();
 
-  if (warp == 0) {
-    if (lane == 0) load_role<D, kF8>(sm, &tmQ, &tmK, &tmV, p, w);
-  } else if (warp == 1) {
-    mma_role<D, kF8>(sm, tmem, p, w);
-  } else if (warp >= 4) {
+  // Register budgets per warpgroup: 104 (load, MMA) + 168 + 168 (softmax) +
+  // 72 (epilogue) = 4 x 128, the launch's share.
+  if (warp < 4) {
+    regs_set<kRegsRoles>();
+    if (warp == 0) {
+      if (lane == 0) load_role<D, kF8>(sm, &tmQ, &tmK, &tmV, p, w);
+    } else if (warp == 1) {
+      mma_role<D, kF8>(sm, tmem, p, w);
+    }
+  } else if (warp < kEpiWarp0) {
+    regs_set<kRegsSoftmax>();
     softmax_role<D, kSplit, kF8>(sm, (warp - 4) >> 2, tmem, p, w);
+  } else {
+    regs_set<kRegsEpi>();
+    epilogue_role<D, kSplit, kF8>(sm, &tmO, tmem, p, w);
   }
   grid_launch_dependents();  // this thread has issued all of its work
 
@@ -1094,12 +1283,14 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
-// [BH][S][D] as a 3-D tensor map with (128 bytes of D) x 128 x 1 boxes and
-// 128-byte swizzle; elements are bf16 (eb = 2) or e4m3 bytes (eb = 1).
-bool encode_3d(CUtensorMap* m, const void* ptr, int D, int S, int64_t BH, int eb = 2) {
+// [BH][S][D] as a 3-D tensor map with (128 bytes of D) x box_rows x 1 boxes
+// and 128-byte swizzle; elements are bf16 (eb = 2), e4m3 bytes (eb = 1) or
+// fp32 (eb = 4).  Loads use 128-row boxes; the forward kernel's O stores use
+// 32-row boxes (one epilogue warp's rows).
+bool encode_3d(CUtensorMap* m, const void* ptr, int D, int S, int64_t BH, int eb = 2, int box_rows = 128) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * eb, static_cast<cuuint64_t>(S) * D * eb};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), 128, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = eb == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -1181,9 +1372,9 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
                      float* o_part, float* lse_part, cudaStream_t stream, float o_scale = 1.f) {
   using C = Cfg<D, kF8>;
   const int64_t BH = static_cast<int64_t>(B) * H;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!encode_3d(&tq, q, D, S_q, BH, C::kEB) || !encode_3d(&tk, k, D, S_kv, BH, C::kEB) ||
-      !encode_3d(&tv, v, D, S_kv, BH, C::kEB))
+      !encode_3d(&tv, v, D, S_kv, BH, C::kEB) || !encode_3d(&to, o, D, S_q, BH, 2, 32))
     return ATTN_ERR_LAUNCH;
   Params prm;
   prm.o = static_cast<uint16_t*>(o);
@@ -1204,12 +1395,13 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   prm.lse_part = lse_part;
   const dim3 grid(static_cast<unsigned>(std::min(prm.n_units, sms)));  // persistent: at most one CTA per SM
   cudaError_t e;
+  const dim3 block(kFwdThreads);
   if constexpr (kF8)
-    e = launch_pdl(attn_fwd_sm103a<D, false, true>, grid, dim3(kThreads), C::kSmemBytes, stream, tq, tk, tv, prm);
+    e = launch_pdl(attn_fwd_sm103a<D, false, true>, grid, block, C::kSmemBytes, stream, tq, tk, tv, to, prm);
   else if (n_splits > 1)
-    e = launch_pdl(attn_fwd_sm103a<D, true, false>, grid, dim3(kThreads), C::kSmemBytes, stream, tq, tk, tv, prm);
+    e = launch_pdl(attn_fwd_sm103a<D, true, false>, grid, block, C::kSmemBytes, stream, tq, tk, tv, to, prm);
   else
-    e = launch_pdl(attn_fwd_sm103a<D, false, false>, grid, dim3(kThreads), C::kSmemBytes, stream, tq, tk, tv, prm);
+    e = launch_pdl(attn_fwd_sm103a<D, false, false>, grid, block, C::kSmemBytes, stream, tq, tk, tv, to, prm);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
