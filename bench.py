@@ -76,6 +76,9 @@ WORKLOADS = {
                                      valid=(8192, 5000)),
     "b1_h32_s32768_d128_qkx2": dict(B=1, H=32, S=32768, D=128, modes=(True, False), seed=6,
                                     q_mult=2.0, k_mult=2.0),
+    # the same kernel and inputs at 8k tokens: small enough for a full ncu capture (201 MB of inputs)
+    "b1_h32_s8192_d128_qkx2": dict(B=1, H=32, S=8192, D=128, modes=(True, False), seed=6,
+                                   q_mult=2.0, k_mult=2.0),
     # one query pair per head against 32k keys: 8 work units for 152 SMs unless the keys are split
     "b1_h8_q256_kv32768_d128_splitkv": dict(B=1, H=8, S=256, S_kv=32768, D=128, modes=(False,), seed=7,
                                             splits="auto"),
