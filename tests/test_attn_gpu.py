@@ -167,14 +167,18 @@ def test_deterministic(dev):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("B,H,graph", [(4, 16, True), (1, 32, True), (2, 8, False)])
-def test_host_forward_equals_one_launch(dev, B, H, graph):
+@pytest.mark.parametrize("B,H,S,graph", [(4, 16, 640, True), (1, 32, 640, True), (2, 8, 640, False),
+                                         (1, 32, 8192, True)])
+def test_host_forward_equals_one_launch(dev, B, H, S, graph):
     # HostForward runs a step as attn_fwd calls on contiguous pieces of the
     # batch, with pinned copies on side streams (captured as a CUDA graph or
     # eager): each row's O and LSE must equal one launch over the whole batch
     import torch
     import io_aware_attention_fwd_gb300 as attn
-    S, D = 640, 64 if B == 4 else 128
+    D = 64 if B == 4 else 128
+    if S > 640:  # long enough for tapered pieces (small first and last ones)
+        from io_aware_attention_fwd_gb300.host import plan_tapered
+        assert plan_tapered(B, H, S, D) is not None
     q, k, v = (parity.to_device(x, dev) for x in qkv(900 + B, B, H, S, S, D))
     kvl = torch.tensor([640, 333], dtype=torch.int32, device=dev) if B == 2 else None
     hf = attn.HostForward(B, H, S, S, D, modes=(False, True), scale=0.1, kv_valid_len=kvl, device=dev, graph=graph)

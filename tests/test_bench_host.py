@@ -74,6 +74,23 @@ def test_auto_piece_count_follows_the_copy_size_rule():
         assert n // auto_pieces(n) >= MIN_PIECE_BYTES
 
 
+def test_tapered_pieces_for_one_long_batch():
+    from io_aware_attention_fwd_gb300.host import plan_tapered
+    # 32k tokens, 32 heads: two-head end pieces (256 units each fill 152 SMs), three middle pieces
+    pl = plan_tapered(1, 32, 32768, 128)
+    assert [nh for _, _, _, nh in pl] == [2, 10, 9, 9, 2]
+    assert [h0 for _, _, h0, _ in pl] == [0, 2, 12, 21, 30]
+    # 4k tokens: an end piece would need 10 heads, too many for a taper; several batches: none
+    assert plan_tapered(1, 32, 4096, 128) is None
+    assert plan_tapered(4, 16, 1024, 64) is None
+    for S in (8192, 16384, 32768, 65536):
+        for H in (8, 16, 32, 64):
+            pl = plan_tapered(1, H, S, 128)
+            if pl is not None:
+                assert sum(nh for *_, nh in pl) == H and pl[0][3] == pl[-1][3]
+                assert all(a[2] + a[3] == b[2] for a, b in zip(pl, pl[1:]))
+
+
 def test_profiled_traffic_needs_the_current_kernel_source(tmp_path, monkeypatch):
     # a profile summary supplies the roofline's DRAM traffic only while its
     # kernel-source hash matches the sources the bench runs
