@@ -55,8 +55,12 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <functional>
 #include <mutex>
+#include <queue>
 #include <type_traits>
+#include <utility>
+#include <vector>
 
 #include "attn_fwd.h"
 
@@ -316,11 +320,16 @@ __device__ __forceinline__ void regs_set() {
   if constexpr (N < kRegsAtLaunch) regs_dec<N>();
   if constexpr (N > kRegsAtLaunch) regs_inc<N>();
 }
-constexpr uint32_t kRegsRoles = 104;    // warps 0-3: TMA producer, MMA issuer (more measured faster)
-constexpr uint32_t kRegsSoftmax = 168;  // warps 4-11
-constexpr uint32_t kRegsEpi = 72;       // warps 12-15
-static_assert(kRegsRoles + 2 * kRegsSoftmax + kRegsEpi == 4 * kRegsAtLaunch,
-              "the budgets share out exactly the launch's registers");
+// Budgets per warpgroup: warps 0-3 (TMA producer, MMA issuer; more measured
+// faster), 4-11 (softmax), 12-15 (epilogue).  With a host schedule the
+// epilogue also walks the unit table and needs 8 more.
+template <bool kTab>
+struct RegBudget {
+  static constexpr uint32_t kRoles = kTab ? 96 : 104;
+  static constexpr uint32_t kSoftmax = 168;
+  static constexpr uint32_t kEpi = kTab ? 80 : 72;
+  static_assert(kRoles + 2 * kSoftmax + kEpi == 4 * kRegsAtLaunch, "the budgets share out exactly the launch's registers");
+};
 
 // --- tcgen05 ---------------------------------------------------------------
 
@@ -598,7 +607,8 @@ struct Unit {
 };
 
 // Unit u -> coordinates.  Causal: the heaviest query pairs of every head come
-// first (longest-processing-time order).  Non-causal: a head's query tiles are
+// first (longest-processing-time order; long causal launches run these units
+// in a host-computed order instead, see build_schedule).  Non-causal: a head's query tiles are
 // adjacent, so the CTAs sharing its K/V run side by side and hit in L2.  With
 // key splitting, the chunks of one query pair are adjacent units; chunk s of
 // a pair whose tiles see at most n kv tiles covers kv tiles
@@ -662,6 +672,28 @@ __device__ __forceinline__ Unit make_unit(const Params& p, int u) {
 // r*G + G-1-c (r odd), which evens out the LPT-ordered causal work.
 __device__ __forceinline__ int unit_of(int r, int c, int G) { return r * G + ((r & 1) ? (G - 1 - c) : c); }
 
+// Per-CTA unit lists computed on the host (see build_schedule): CTA c runs
+// units unit[off[c]] .. unit[off[c + 1] - 1], in that order, each encoded as
+// make_unit expects.  Passed by value as a kernel parameter.
+constexpr int kTabMaxCtas = 256;
+constexpr int kTabMaxUnits = 14336;
+struct UnitTable {
+  uint16_t off[kTabMaxCtas + 1];
+  uint16_t unit[kTabMaxUnits];
+};
+
+// The work units of this CTA, in order: from a host table, or else the
+// static snake over the formula order (which may name units past the end;
+// callers skip those).
+struct UnitSeq {
+  const UnitTable* tab;
+  int G, cta, n_units;
+  __device__ UnitSeq(const Params& p, const UnitTable* t)
+      : tab(t), G(static_cast<int>(gridDim.x)), cta(static_cast<int>(blockIdx.x)), n_units(p.n_units) {}
+  __device__ int size() const { return tab ? tab->off[cta + 1] - tab->off[cta] : (n_units + G - 1) / G; }
+  __device__ int at(int r) const { return tab ? static_cast<int>(tab->unit[tab->off[cta] + r]) : unit_of(r, cta, G); }
+};
+
 // ---------------------------------------------------------------------------
 // Roles
 // ---------------------------------------------------------------------------
@@ -670,15 +702,15 @@ __device__ __forceinline__ int unit_of(int r, int c, int G) { return r * G + ((r
 // K/V item `it` (counted across units) lives in slot it % kSlots.
 template <int D, bool kF8>
 __device__ void load_role(const Smem<D, kF8>& sm, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                          const CUtensorMap* tmV, const Params& p, const WaitCtx& w) {
+                          const CUtensorMap* tmV, const Params& p, const UnitTable* tab, const WaitCtx& w) {
   using C = Cfg<D, kF8>;
-  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
-  const int rounds = (p.n_units + G - 1) / G;
+  const UnitSeq us(p, tab);
+  const int rounds = us.size();
   int it = 0;  // K/V items issued
   int k = 0;   // units whose Q was issued
   bool ok = true;
   for (int r = 0; r < rounds && ok; ++r) {
-    const int u = unit_of(r, cta, G);
+    const int u = us.at(r);
     if (u >= p.n_units) continue;
     const Unit un = make_unit(p, u);
     if (k > 0) {  // the previous unit's last S MMAs have read both Q tiles
@@ -725,7 +757,8 @@ __device__ void load_role(const Smem<D, kF8>& sm, const CUtensorMap* tmQ, const 
 // the epilogue warpgroup has read the previous unit's O_t out of TMEM
 // (o_free).
 template <int D, bool kF8>
-__device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p, const WaitCtx& w) {
+__device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p, const UnitTable* tab,
+                         const WaitCtx& w) {
   using C = Cfg<D, kF8>;
   constexpr uint32_t idesc_s = make_idesc(kBM, kBN, false, false, kF8);
   constexpr uint32_t idesc_pv = make_idesc(kBM, D, false, true, kF8);
@@ -736,14 +769,14 @@ __device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p,
   const uint64_t kd0 = sdesc_kmajor_sw128(sm.slot(0));
   const uint64_t vd0 = sdesc_mnmajor_sw128(sm.slot(0), kPanelBytes);
   constexpr uint64_t kSlotStep = C::kTileBytes >> 4;  // descriptor distance between slots
-  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
-  const int rounds = (p.n_units + G - 1) / G;
+  const UnitSeq us(p, tab);
+  const int rounds = us.size();
   int it = 0;                // K/V items consumed
   int k = 0;                 // units started
   int pc[kQTiles] = {0, 0};  // P_full phases consumed
   bool ok = true, issued = false;
   for (int r = 0; r < rounds && ok; ++r) {
-    const int u = unit_of(r, cta, G);
+    const int u = us.at(r);
     if (u >= p.n_units) continue;
     const Unit un = make_unit(p, u);
     const int sk0 = it % C::kSlots;
@@ -805,21 +838,22 @@ __device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p,
 // unit it hands the row's statistics (m, l) to the epilogue warpgroup, which
 // normalises and stores O and LSE.
 template <int D, bool kSplit, bool kF8>
-__device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const Params& p, const WaitCtx& w) {
+__device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const Params& p, const UnitTable* tab,
+                             const WaitCtx& w) {
   using C = Cfg<D, kF8>;
   const int r = static_cast<int>(threadIdx.x) - kBM * (1 + t);  // row in tile == TMEM lane
   const int qw = r >> 5;                                         // lane quarter (warp % 4)
   const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
   const uint32_t tS = tmem + lane_off + t * kBN;
   const float c = p.scale_log2;
-  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
-  const int rounds = (p.n_units + G - 1) / G;
+  const UnitSeq us(p, tab);
+  const int rounds = us.size();
   int cnt = 0;    // kv tiles this query tile has processed (S_full / O_done phases)
   int sbase = 0;  // softmax steps of both query tiles in this CTA's earlier units
   int k = 0;      // units finished
   bool ok = true;
   for (int rr = 0; rr < rounds && ok; ++rr) {
-    const int u = unit_of(rr, cta, G);
+    const int u = us.at(rr);
     if (u >= p.n_units) continue;
     const Unit un = make_unit(p, u);
     const int qs = un.q0 + t * kBM;
@@ -965,20 +999,20 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
 // the softmax warps are already on the next unit's first steps.
 template <int D, bool kSplit, bool kF8>
 __device__ void epilogue_role(const Smem<D, kF8>& sm, const CUtensorMap* tmO, uint32_t tmem, const Params& p,
-                              const WaitCtx& w) {
+                              const UnitTable* tab, const WaitCtx& w) {
   using C = Cfg<D, kF8>;
   const int qw = static_cast<int>(threadIdx.x >> 5) & 3;
   const int lane = static_cast<int>(threadIdx.x & 31);
   const int rt = qw * 32 + lane;  // row within a query tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
   const uint32_t stage = sm.stage(qw);
-  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
-  const int rounds = (p.n_units + G - 1) / G;
+  const UnitSeq us(p, tab);
+  const int rounds = us.size();
   int cnt[kQTiles] = {0, 0};  // P.V products of each query tile in earlier units
   int k = 0;                  // units finished
   bool ok = true;
   for (int rr = 0; rr < rounds && ok; ++rr) {
-    const int u = unit_of(rr, cta, G);
+    const int u = us.at(rr);
     if (u >= p.n_units) continue;
     const Unit un = make_unit(p, u);
     // Epilogues of this unit's two query tiles.
@@ -1077,11 +1111,9 @@ __device__ void epilogue_role(const Smem<D, kF8>& sm, const CUtensorMap* tmO, ui
   if (lane == 0) bulk_wait_all();  // every O store of this warp is complete before the CTA exits
 }
 
-template <int D, bool kSplit, bool kF8>
-__global__ void __launch_bounds__(kFwdThreads, 1)
-    attn_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const Params p) {
+template <int D, bool kSplit, bool kF8, bool kTab>
+__device__ __forceinline__ void attn_fwd_body(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                              const CUtensorMap& tmO, const Params& p, const UnitTable* tab) {
   using C = Cfg<D, kF8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -1130,21 +1162,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // kernel's outputs (Q, K, V, kv_valid_len) and writes O and LSE.
   grid_dependency_wait();
 
-  // Register budgets per warpgroup: 104 (load, MMA) + 168 + 168 (softmax) +
-  // 72 (epilogue) = 4 x 128, the launch's share.
+  // Register budgets per warpgroup (RegBudget): they add up to 4 x 128, the
+  // launch's share.
+  using R = RegBudget<kTab>;
   if (warp < 4) {
-    regs_set<kRegsRoles>();
+    regs_set<R::kRoles>();
     if (warp == 0) {
-      if (lane == 0) load_role<D, kF8>(sm, &tmQ, &tmK, &tmV, p, w);
+      if (lane == 0) load_role<D, kF8>(sm, &tmQ, &tmK, &tmV, p, tab, w);
     } else if (warp == 1) {
-      mma_role<D, kF8>(sm, tmem, p, w);
+      mma_role<D, kF8>(sm, tmem, p, tab, w);
     }
   } else if (warp < kEpiWarp0) {
-    regs_set<kRegsSoftmax>();
-    softmax_role<D, kSplit, kF8>(sm, (warp - 4) >> 2, tmem, p, w);
+    regs_set<R::kSoftmax>();
+    softmax_role<D, kSplit, kF8>(sm, (warp - 4) >> 2, tmem, p, tab, w);
   } else {
-    regs_set<kRegsEpi>();
-    epilogue_role<D, kSplit, kF8>(sm, &tmO, tmem, p, w);
+    regs_set<R::kEpi>();
+    epilogue_role<D, kSplit, kF8>(sm, &tmO, tmem, p, tab, w);
   }
   grid_launch_dependents();  // this thread has issued all of its work
 
@@ -1155,6 +1188,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// The forward kernel: units in the static snake over the formula order.
+template <int D, bool kSplit, bool kF8>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_sm103a(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const Params p) {
+  attn_fwd_body<D, kSplit, kF8, false>(tmQ, tmK, tmV, tmO, p, nullptr);
+}
+
+// The same kernel with each CTA's units listed by the host (long causal
+// launches: see build_schedule).
+template <int D, bool kF8>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_sm103a_sched(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                          const Params p, const __grid_constant__ UnitTable tab) {
+  attn_fwd_body<D, false, kF8, true>(tmQ, tmK, tmV, tmO, p, &tab);
 }
 
 // S_kv == 0: every row has no allowed key -> O = 0, LSE = -inf.
@@ -1351,6 +1403,12 @@ attn_status_t prepare_device(int dev) {
                            Cfg<128, false>::kSmemBytes) != cudaSuccess ||
       cudaFuncSetAttribute(attn_fwd_sm103a<128, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128, true>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a_sched<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<64, false>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a_sched<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128, false>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_fwd_sm103a_sched<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128, true>::kSmemBytes) != cudaSuccess ||
       cudaFuncSetAttribute(attn_bwd_sm103a<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            BwdCfg<64>::kSmemBytes) != cudaSuccess ||
       cudaFuncSetAttribute(attn_bwd_sm103a<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1362,6 +1420,86 @@ attn_status_t prepare_device(int dev) {
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Host-computed schedule for long causal launches.  The longest-first order
+// balances the CTAs' work but keeps every head's units live at once, at
+// different key positions; when the heads' K and V together outgrow L2
+// (here: more than kSchedL2Bytes), every unit then streams its keys from
+// DRAM (measured at 32k tokens, 32 heads: 11 GB per launch for 1.08 GB of
+// inputs and outputs).  Instead, units are taken head by head, heaviest
+// query pair first, and the last few heads (whose K and V fit in
+// kSchedL2Bytes together) interleaved longest first, so the tail still
+// balances; each unit goes to the CTA that is free earliest (greedy list
+// scheduling with a unit costing its kv steps plus one).  A handful of heads
+// is live at any time.  In simulation at 32k this keeps the balance at
+// 0.995 (longest-first: 0.999).
+constexpr int64_t kSchedL2Bytes = 64ll << 20;
+
+bool schedule_wanted(int causal, const int32_t* kv_valid_len, int n_splits, int64_t BH, int S_kv, int D, int eb,
+                     int n_units, int grid) {
+  return causal && kv_valid_len == nullptr && n_splits == 1 && BH * S_kv * static_cast<int64_t>(D) * eb * 2 > kSchedL2Bytes &&
+         n_units <= kTabMaxUnits && grid <= kTabMaxCtas;
+}
+
+void build_schedule(int BH, int n_pairs, int S_q, int S_kv, int D, int eb, int G, UnitTable* tab) {
+  const int n_units = BH * n_pairs;
+  // kv steps of unit u (encoded as make_unit decodes it when causal)
+  auto steps = [&](int u) {
+    const int pair = n_pairs - 1 - u / BH;
+    int n = 1;
+    for (int t = 0; t < kQTiles; ++t) {
+      const int qs = pair * kRowsPerUnit + t * kBM;
+      const int lim = qs >= S_q ? 1 : std::min(S_kv, std::min(qs + kBM, S_q));
+      n = std::max(n, (lim + kBN - 1) / kBN);
+    }
+    return n;
+  };
+  const int64_t head_kv = static_cast<int64_t>(S_kv) * D * eb * 2;
+  const int k_tail = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(BH, kSchedL2Bytes / head_kv)));
+  std::vector<int> order;
+  order.reserve(n_units);
+  for (int bh = 0; bh < BH - k_tail; ++bh)
+    for (int pair = n_pairs - 1; pair >= 0; --pair) order.push_back((n_pairs - 1 - pair) * BH + bh);
+  for (int pair = n_pairs - 1; pair >= 0; --pair)
+    for (int bh = BH - k_tail; bh < BH; ++bh) order.push_back((n_pairs - 1 - pair) * BH + bh);
+  using Slot = std::pair<int64_t, int>;  // (work so far, CTA): the earliest free, lowest index first
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+  for (int c = 0; c < G; ++c) free_at.push({0, c});
+  std::vector<std::vector<uint16_t>> lists(G);
+  for (const int u : order) {
+    const Slot sl = free_at.top();
+    free_at.pop();
+    lists[sl.second].push_back(static_cast<uint16_t>(u));
+    free_at.push({sl.first + steps(u) + 1, sl.second});
+  }
+  int pos = 0;
+  for (int c = 0; c < G; ++c) {
+    tab->off[c] = static_cast<uint16_t>(pos);
+    for (const uint16_t u : lists[c]) tab->unit[pos++] = u;
+  }
+  tab->off[G] = static_cast<uint16_t>(pos);
+}
+
+// The last few schedules, by shape (a schedule is a pure function of it).
+struct SchedEntry {
+  int key[7];
+  UnitTable tab;
+};
+std::mutex g_sched_mu;
+std::vector<SchedEntry> g_sched_cache;
+
+const UnitTable* schedule_for(int BH, int n_pairs, int S_q, int S_kv, int D, int eb, int G) {
+  const int key[7] = {BH, n_pairs, S_q, S_kv, D, eb, G};
+  std::lock_guard<std::mutex> lock(g_sched_mu);
+  for (const SchedEntry& e : g_sched_cache)
+    if (std::equal(key, key + 7, e.key)) return &e.tab;
+  if (g_sched_cache.size() >= 8) g_sched_cache.erase(g_sched_cache.begin());
+  g_sched_cache.emplace_back();
+  SchedEntry& e = g_sched_cache.back();
+  std::copy(key, key + 7, e.key);
+  build_schedule(BH, n_pairs, S_q, S_kv, D, eb, G, &e.tab);
+  return &e.tab;
+}
 
 // Launches the attention kernel; with n_splits > 1 it writes fp32 partials to
 // o_part / lse_part instead of o / lse.  kF8: e4m3 Q, K, V; `scale` then
@@ -1393,9 +1531,20 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   prm.o_scale = o_scale;
   prm.o_part = o_part;
   prm.lse_part = lse_part;
-  const dim3 grid(static_cast<unsigned>(std::min(prm.n_units, sms)));  // persistent: at most one CTA per SM
+  const int G = std::min(prm.n_units, sms);  // persistent: at most one CTA per SM
+  const dim3 grid(static_cast<unsigned>(G));
   cudaError_t e;
   const dim3 block(kFwdThreads);
+  if (schedule_wanted(causal, kv_valid_len, n_splits, BH, S_kv, D, C::kEB, prm.n_units, G)) {
+    UnitTable tab;  // copied into the launch's parameters
+    {
+      const UnitTable* t = schedule_for(static_cast<int>(BH), prm.n_pairs, S_q, S_kv, D, C::kEB, G);
+      std::lock_guard<std::mutex> lock(g_sched_mu);  // the cache entry may be replaced by another thread
+      tab = *t;
+    }
+    e = launch_pdl(attn_fwd_sm103a_sched<D, kF8>, grid, block, C::kSmemBytes, stream, tq, tk, tv, to, prm, tab);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+  }
   if constexpr (kF8)
     e = launch_pdl(attn_fwd_sm103a<D, false, true>, grid, block, C::kSmemBytes, stream, tq, tk, tv, to, prm);
   else if (n_splits > 1)
