@@ -134,6 +134,17 @@ def alg_bytes(w, causal):
     return H * (2 * S * D * 2 * B + 2 * kv * D * 2 + S * 4 * B)
 
 
+def fwd_kernel_name(w) -> str:
+    """The bf16 forward kernel(s) a step of workload ``w`` launches: causal
+    launches whose K and V together exceed 64 MiB (and that have no key
+    padding) run the table-scheduled instantiation of the same kernel body."""
+    D = w["D"]
+    kv_bytes = w["B"] * w["H"] * s_kv(w) * D * 2 * 2
+    if True in w["modes"] and not w.get("valid") and kv_bytes > 64 << 20:
+        return f"attn_fwd_sm103a<{D}> (causal: attn_fwd_sm103a_sched<{D}>, host-built unit order)"
+    return f"attn_fwd_sm103a<{D}>"
+
+
 def workload_config(name, w, world):
     """The ``config`` object of the JSON line; both arms print the same one."""
     D = w["D"]
@@ -628,7 +639,7 @@ def main():
                      "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
                      "alg_bytes_per_launch": sum(alg_bytes(w, c) for c in modes) / n_l,
                      "kernel": (f"attn_bwd_prep + attn_bwd_sm103a<{D}> + attn_bwd_dq_convert (one call)" if bwd else
-                                f"attn_fwd_sm103a<{D}, e4m3>" if fp8 else f"attn_fwd_sm103a<{D}>" if splits == 1 else
+                                f"attn_fwd_sm103a<{D}, e4m3>" if fp8 else fwd_kernel_name(w) if splits == 1 else
                                 f"attn_fwd_sm103a<{D}, split> + attn_merge_kernel<{D}> (one call, both timed)"),
                      "peak_source": peak_src},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

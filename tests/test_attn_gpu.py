@@ -83,6 +83,17 @@ def test_c5_32k(c5, causal):
     parity.check_against_oracle(q, k, v, 1 / math.sqrt(128), causal, rows=rows, tensors=t)
 
 
+@pytest.mark.parametrize("D,S,H", [(128, 9000, 16), (64, 17000, 16)])
+def test_long_causal_host_schedule_ragged(dev, D, S, H):
+    # Causal launches whose heads' K and V exceed 64 MB run the units in a
+    # host-computed order (a per-CTA unit table); here with a ragged last
+    # tile and a head count that does not divide the SM count.
+    assert H * S * D * 2 * 2 > 64 << 20
+    q, k, v = qkv(950 + D, 1, H, S, S, D)
+    rows = parity.sampled_rows(950 + D, 1, H, S, 64, must_include=[0, 1, 255, 256, S // 2, S - 129, S - 1])
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(D), True, rows=rows)
+
+
 # --- edge cases ----------------------------------------------------------------
 
 @pytest.mark.parametrize("D", [64, 128])
