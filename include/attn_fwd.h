@@ -164,6 +164,36 @@ uint64_t attn_fwd_splitkv_workspace_bytes(int B, int H, int S_q, int D, int n_sp
 int attn_fwd_splitkv_suggest(int B, int H, int S_q, int S_kv, int D, int causal);
 
 /*
+ * attn_fwd_schedule -- the order in which attn_fwd runs the work units of a
+ * causal launch of this shape on a device with `sms` SMs, for inspection.
+ * Host only: touches no device and launches nothing.
+ *
+ * A work unit is a pair of 128-row query tiles (256 rows) of one (batch,
+ * head): with BH = B*H and n_pairs = ceil(S_q / 256), unit u covers query
+ * rows [256 p, 256 p + 256) of head bh = u % BH, where p = n_pairs - 1 -
+ * u / BH.  A causal launch without key padding whose K and V together take
+ * more than 64 MiB (B*H*S_kv*D*elem_bytes*2 bytes) runs its units in a
+ * host-built order: the heads one after another, heaviest query pair first,
+ * with the last heads whose K and V fit in 64 MiB interleaved, each unit
+ * going to the CTA that is free earliest (greedy list scheduling, a unit
+ * costing its kv tiles plus one).  This keeps a few heads' K and V in L2
+ * instead of every head's.  Other launches take the units in a fixed
+ * longest-first order and have no table.
+ *
+ *   elem_bytes  2 for bf16 (attn_fwd), 1 for e4m3 (attn_fwd_fp8)
+ *   off         host uint16 [min(units, sms) + 1], written: CTA c runs
+ *               unit[off[c]] .. unit[off[c + 1] - 1], in that order
+ *   unit        host uint16 [cap], written: B*H*n_pairs unit indices
+ *
+ * Returns the number of units written, 0 when the shape has no host-built
+ * order (nothing written), or -1 for an invalid argument (B, H, S_q or S_kv
+ * below 1, D not 64 or 128, elem_bytes not 1 or 2, sms below 1, a NULL
+ * pointer, more units than fit an int) or a `cap` below the unit count.
+ */
+int attn_fwd_schedule(int B, int H, int S_q, int S_kv, int D, int elem_bytes, int sms, uint16_t* off,
+                      uint16_t* unit, int cap);
+
+/*
  * attn_merge -- combine attention results computed over disjoint key sets:
  *   lse = ln sum_k exp(lse_k),  O = sum_k exp(lse_k - lse) O_k.
  *   o_parts    device fp32 [n_parts][rows][D], 16-byte aligned

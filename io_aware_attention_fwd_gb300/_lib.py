@@ -21,7 +21,7 @@ ATTN_ERR_DEVICE = 6
 
 # every extern "C" function include/attn_fwd.h declares
 EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
-            "attn_fwd_splitkv_suggest", "attn_merge", "attn_fwd_splitkv_static", "attn_status_str", "attn_fwd_debug_status",
+            "attn_fwd_splitkv_suggest", "attn_fwd_schedule", "attn_merge", "attn_fwd_splitkv_static", "attn_status_str", "attn_fwd_debug_status",
             "attn_watchdog_selftest", "attn_fwd_abi_version")
 
 _lock = threading.Lock()
@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
             lib.attn_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
             lib.attn_fwd_splitkv_suggest.restype = i
             lib.attn_fwd_splitkv_suggest.argtypes = [i, i, i, i, i, i]
+            lib.attn_fwd_schedule.restype = i
+            lib.attn_fwd_schedule.argtypes = [i, i, i, i, i, i, i, p, p, i]
             f = ctypes.c_float
             lib.attn_bwd.restype = i
             lib.attn_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, i, p, p, u64, p]
@@ -161,6 +163,24 @@ def attn_fwd_splitkv_workspace_bytes(B: int, H: int, S_q: int, D: int, n_splits:
 def attn_fwd_splitkv_suggest(B: int, H: int, S_q: int, S_kv: int, D: int, causal: bool) -> int:
     return int(load().attn_fwd_splitkv_suggest(int(B), int(H), int(S_q), int(S_kv), int(D),
                                                int(bool(causal))))
+
+
+def attn_fwd_schedule(B: int, H: int, S_q: int, S_kv: int, D: int, elem_bytes: int, sms: int):
+    """The host-built unit order of a causal launch of this shape (see
+    include/attn_fwd.h): (off, unit) as lists, CTA c running
+    unit[off[c]:off[c + 1]]; None where the launch has no such order."""
+    n_pairs = -(-int(S_q) // 256)
+    cap = max(1, int(B) * int(H) * n_pairs)
+    off = (ctypes.c_uint16 * (max(1, int(sms)) + 1))()
+    unit = (ctypes.c_uint16 * cap)()
+    n = load().attn_fwd_schedule(int(B), int(H), int(S_q), int(S_kv), int(D), int(elem_bytes), int(sms),
+                                 ctypes.addressof(off), ctypes.addressof(unit), cap)
+    if n < 0:
+        raise ValueError("attn_fwd_schedule: invalid arguments")
+    if n == 0:
+        return None
+    G = min(n, int(sms))
+    return list(off[:G + 1]), list(unit[:n])
 
 
 def attn_merge(o_parts, lse_parts, n_parts: int, rows: int, D: int, o, lse, stream=None) -> None:

@@ -70,6 +70,7 @@ constexpr int kBM = 128;              // query rows per softmax tile (TMEM lanes
 constexpr int kBN = 128;              // keys per kv tile
 constexpr int kQTiles = 2;            // query tiles per work unit
 constexpr int kRowsPerUnit = kBM * kQTiles;
+constexpr int kListMax = 1024;        // units one CTA may be given by a host-built order
 constexpr int kThreads = 384;         // backward kernel: warps 0-3 roles, 4-11 key rows / dQ
 constexpr int kFwdThreads = 512;      // forward kernel: warps 0-3 roles, 4-7 / 8-11 softmax, 12-15 epilogue
 constexpr int kEpiWarp0 = 12;         // first warp of the forward kernel's epilogue warpgroup
@@ -108,8 +109,9 @@ struct Cfg {
   // barriers: q_full | q_free[2] | full[kSlots] | empty[kSlots] | s_full[2] | p_full[2] |
   //           o_done[2] | drain | turn | o_free[2] | epi[2]
   static constexpr int kNumBars = 1 + kQTiles + 2 * kSlots + 3 * kQTiles + 2 + 2 * kQTiles;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] tmem base, [1] abort flag
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1024 B alignment
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] tmem base, [1] abort flag, [2] listed units
+  static constexpr int kListOff = kMiscOff + 16;           // uint16 [kListMax]: this CTA's units (host order)
+  static constexpr int kSmemBytes = kListOff + 2 * kListMax + 1024;  // + slack for 1024 B alignment
   static constexpr int kOCol0 = kQTiles * kBN;             // first O column in TMEM
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
@@ -267,6 +269,25 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// L2 cache policy for the bulk copies of data read or written once (Q, O):
+// those lines go first, so they do not push K and V, which many units
+// reread, out of L2.  Measured on GB300 at 4k tokens, 32 heads, causal: DRAM
+// reads 122 MB instead of 137 MB (Q + K + V = 101 MB), at the same speed; an
+// evict-last policy on the K/V loads changed nothing.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y,
+                                                 int z, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol)
+      : "memory");
+}
+
 // Programmatic dependent launch.  The kernel is launched so that it may start
 // while the previous kernel in its stream is still finishing: it builds its
 // on-chip state (barriers, tensor memory) first and waits here before its
@@ -280,11 +301,13 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// shared -> global tensor copy of one box (coordinates of its first element)
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+// shared -> global tensor copy of one box (coordinates of its first element),
+// with an L2 cache policy
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* m, uint32_t src, int x, int y, int z,
+                                                  uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
                    reinterpret_cast<uint64_t>(m)),
-               "r"(src), "r"(x), "r"(y), "r"(z)
+               "r"(src), "r"(x), "r"(y), "r"(z), "l"(pol)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -321,15 +344,15 @@ __device__ __forceinline__ void regs_set() {
   if constexpr (N > kRegsAtLaunch) regs_inc<N>();
 }
 // Budgets per warpgroup: warps 0-3 (TMA producer, MMA issuer; more measured
-// faster), 4-11 (softmax), 12-15 (epilogue).  With a host schedule the
-// epilogue also walks the unit table and needs 8 more.
-template <bool kTab>
-struct RegBudget {
-  static constexpr uint32_t kRoles = kTab ? 96 : 104;
-  static constexpr uint32_t kSoftmax = 168;
-  static constexpr uint32_t kEpi = kTab ? 80 : 72;
-  static_assert(kRoles + 2 * kSoftmax + kEpi == 4 * kRegsAtLaunch, "the budgets share out exactly the launch's registers");
-};
+// faster), 4-11 (softmax), 12-15 (epilogue).  With a host-built unit order
+// ptxas reports an 8-byte spill at these budgets (a unit index read from
+// shared memory cannot be recomputed); 96 / 80 left 4 bytes and measured
+// slower, so both instances keep these.
+constexpr uint32_t kRegsRoles = 104;
+constexpr uint32_t kRegsSoftmax = 168;
+constexpr uint32_t kRegsEpi = 72;
+static_assert(kRegsRoles + 2 * kRegsSoftmax + kRegsEpi == 4 * kRegsAtLaunch,
+              "the budgets share out exactly the launch's registers");
 
 // --- tcgen05 ---------------------------------------------------------------
 
@@ -580,6 +603,8 @@ struct Smem {
   __device__ float2* stat(int t) const { return reinterpret_cast<float2*>(ptr + Cfg<D, kF8>::kStatOff) + t * kBM; }
   __device__ uint32_t slot(int s) const { return base + Cfg<D, kF8>::kSlotOff + s * Cfg<D, kF8>::kTileBytes; }
   __device__ uint32_t bar(int i) const { return base + Cfg<D, kF8>::kBarOff + 8 * i; }
+  __device__ uint32_t list() const { return base + Cfg<D, kF8>::kListOff; }
+  __device__ int listed() const { return static_cast<int>(reinterpret_cast<const volatile uint32_t*>(ptr + Cfg<D, kF8>::kMiscOff)[2]); }
   __device__ uint32_t bar_q() const { return bar(0); }
   __device__ uint32_t bar_qfree(int t) const { return bar(1 + t); }
   __device__ uint32_t bar_full(int s) const { return bar(1 + kQTiles + s); }
@@ -674,7 +699,8 @@ __device__ __forceinline__ int unit_of(int r, int c, int G) { return r * G + ((r
 
 // Per-CTA unit lists computed on the host (see build_schedule): CTA c runs
 // units unit[off[c]] .. unit[off[c + 1] - 1], in that order, each encoded as
-// make_unit expects.  Passed by value as a kernel parameter.
+// make_unit expects.  Passed by value as a kernel parameter; each CTA copies
+// its own list (at most kListMax units) into shared memory before it starts.
 constexpr int kTabMaxCtas = 256;
 constexpr int kTabMaxUnits = 14336;
 struct UnitTable {
@@ -682,16 +708,31 @@ struct UnitTable {
   uint16_t unit[kTabMaxUnits];
 };
 
-// The work units of this CTA, in order: from a host table, or else the
-// static snake over the formula order (which may name units past the end;
-// callers skip those).
+// The work units of this CTA, in order: with kTab, the list the host built
+// (copied into shared memory at kernel start), else the static snake over
+// the formula order (which may name units past the end; callers skip those).
+__device__ __forceinline__ int ld_shared_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return static_cast<int>(v);
+}
+
+template <bool kTab>
 struct UnitSeq {
-  const UnitTable* tab;
-  int G, cta, n_units;
-  __device__ UnitSeq(const Params& p, const UnitTable* t)
-      : tab(t), G(static_cast<int>(gridDim.x)), cta(static_cast<int>(blockIdx.x)), n_units(p.n_units) {}
-  __device__ int size() const { return tab ? tab->off[cta + 1] - tab->off[cta] : (n_units + G - 1) / G; }
-  __device__ int at(int r) const { return tab ? static_cast<int>(tab->unit[tab->off[cta] + r]) : unit_of(r, cta, G); }
+  uint32_t list;
+  int n, G, cta;
+  template <int D, bool kF8>
+  __device__ UnitSeq(const Params& p, const Smem<D, kF8>& sm)
+      : list(sm.list()), G(static_cast<int>(gridDim.x)), cta(static_cast<int>(blockIdx.x)) {
+    n = kTab ? sm.listed() : (p.n_units + G - 1) / G;
+  }
+  __device__ int size() const { return n; }
+  __device__ int at(int r) const {
+    if constexpr (kTab)
+      return ld_shared_u16(list + 2u * static_cast<uint32_t>(r));
+    else
+      return unit_of(r, cta, G);
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -700,15 +741,16 @@ struct UnitSeq {
 
 // TMA producer (one thread).  Per unit: Q_0, Q_1, then K_0, V_0, K_1, V_1, ...;
 // K/V item `it` (counted across units) lives in slot it % kSlots.
-template <int D, bool kF8>
+template <int D, bool kF8, bool kTab>
 __device__ void load_role(const Smem<D, kF8>& sm, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                          const CUtensorMap* tmV, const Params& p, const UnitTable* tab, const WaitCtx& w) {
+                          const CUtensorMap* tmV, const Params& p, const WaitCtx& w) {
   using C = Cfg<D, kF8>;
-  const UnitSeq us(p, tab);
+  const UnitSeq<kTab> us(p, sm);
   const int rounds = us.size();
   int it = 0;  // K/V items issued
   int k = 0;   // units whose Q was issued
   bool ok = true;
+  const uint64_t pol_first = l2_evict_first();  // for Q
   for (int r = 0; r < rounds && ok; ++r) {
     const int u = us.at(r);
     if (u >= p.n_units) continue;
@@ -722,7 +764,7 @@ __device__ void load_role(const Smem<D, kF8>& sm, const CUtensorMap* tmQ, const 
       int y = un.q0 + t * kBM;
       if (y >= p.S_q) y = un.q0;  // a tile wholly past the end reloads tile 0 (never stored)
       for (int pn = 0; pn < C::kPanels; ++pn)
-        tma_load_3d(sm.q(t) + pn * kPanelBytes, tmQ, sm.bar_q(), pn * C::kBoxCols, y, un.bh);
+        tma_load_3d_hint(sm.q(t) + pn * kPanelBytes, tmQ, sm.bar_q(), pn * C::kBoxCols, y, un.bh, pol_first);
     }
     ++k;
     for (int j = 0; j < un.n && ok; ++j) {
@@ -756,9 +798,8 @@ __device__ void load_role(const Smem<D, kF8>& sm, const CUtensorMap* tmQ, const 
 // Each P_t V waits for P_t (softmax); the first of a unit also waits until
 // the epilogue warpgroup has read the previous unit's O_t out of TMEM
 // (o_free).
-template <int D, bool kF8>
-__device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p, const UnitTable* tab,
-                         const WaitCtx& w) {
+template <int D, bool kF8, bool kTab>
+__device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p, const WaitCtx& w) {
   using C = Cfg<D, kF8>;
   constexpr uint32_t idesc_s = make_idesc(kBM, kBN, false, false, kF8);
   constexpr uint32_t idesc_pv = make_idesc(kBM, D, false, true, kF8);
@@ -769,7 +810,7 @@ __device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p,
   const uint64_t kd0 = sdesc_kmajor_sw128(sm.slot(0));
   const uint64_t vd0 = sdesc_mnmajor_sw128(sm.slot(0), kPanelBytes);
   constexpr uint64_t kSlotStep = C::kTileBytes >> 4;  // descriptor distance between slots
-  const UnitSeq us(p, tab);
+  const UnitSeq<kTab> us(p, sm);
   const int rounds = us.size();
   int it = 0;                // K/V items consumed
   int k = 0;                 // units started
@@ -837,16 +878,15 @@ __device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p,
 // rescales O in TMEM before releasing P (lazy correction).  At the end of a
 // unit it hands the row's statistics (m, l) to the epilogue warpgroup, which
 // normalises and stores O and LSE.
-template <int D, bool kSplit, bool kF8>
-__device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const Params& p, const UnitTable* tab,
-                             const WaitCtx& w) {
+template <int D, bool kSplit, bool kF8, bool kTab>
+__device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const Params& p, const WaitCtx& w) {
   using C = Cfg<D, kF8>;
   const int r = static_cast<int>(threadIdx.x) - kBM * (1 + t);  // row in tile == TMEM lane
   const int qw = r >> 5;                                         // lane quarter (warp % 4)
   const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
   const uint32_t tS = tmem + lane_off + t * kBN;
   const float c = p.scale_log2;
-  const UnitSeq us(p, tab);
+  const UnitSeq<kTab> us(p, sm);
   const int rounds = us.size();
   int cnt = 0;    // kv tiles this query tile has processed (S_full / O_done phases)
   int sbase = 0;  // softmax steps of both query tiles in this CTA's earlier units
@@ -997,16 +1037,16 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
 // row.  With key splitting it writes the fp32 partial O (divided by the
 // chunk's own l) and the chunk's LSE to the workspace instead.  Meanwhile
 // the softmax warps are already on the next unit's first steps.
-template <int D, bool kSplit, bool kF8>
+template <int D, bool kSplit, bool kF8, bool kTab>
 __device__ void epilogue_role(const Smem<D, kF8>& sm, const CUtensorMap* tmO, uint32_t tmem, const Params& p,
-                              const UnitTable* tab, const WaitCtx& w) {
+                              const WaitCtx& w) {
   using C = Cfg<D, kF8>;
   const int qw = static_cast<int>(threadIdx.x >> 5) & 3;
   const int lane = static_cast<int>(threadIdx.x & 31);
   const int rt = qw * 32 + lane;  // row within a query tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
   const uint32_t stage = sm.stage(qw);
-  const UnitSeq us(p, tab);
+  const UnitSeq<kTab> us(p, sm);
   const int rounds = us.size();
   int cnt[kQTiles] = {0, 0};  // P.V products of each query tile in earlier units
   int k = 0;                  // units finished
@@ -1099,7 +1139,7 @@ __device__ void epilogue_role(const Smem<D, kF8>& sm, const CUtensorMap* tmO, ui
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (row0 < p.S_q) tma_store_3d(tmO, stage, pn * 64, row0, un.bh);
+            if (row0 < p.S_q) tma_store_3d_hint(tmO, stage, pn * 64, row0, un.bh, l2_evict_first());
             bulk_commit();
           }
         }
@@ -1142,6 +1182,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap& tmQ, const CUte
     mbar_init(sm.bar_drain(), 1);
     mbar_init(sm.bar_turn(), kBM);
     misc[1] = 0u;
+    if (kTab) misc[2] = static_cast<uint32_t>(tab->off[blockIdx.x + 1] - tab->off[blockIdx.x]);
     fence_barrier_init();
   } else if (threadIdx.x == 32) {
     tma_prefetch_desc(&tmQ);  // the tensor maps are kernel parameters, not
@@ -1153,6 +1194,11 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap& tmQ, const CUte
     tmem_alloc(base + C::kMiscOff, kTmemCols);
     tmem_relinquish();
   }
+  if (kTab) {  // this CTA's units, from the kernel parameters into shared memory
+    const int o0 = tab->off[blockIdx.x], n = tab->off[blockIdx.x + 1] - o0;
+    uint16_t* list = reinterpret_cast<uint16_t*>(smem + C::kListOff);
+    for (int i = static_cast<int>(threadIdx.x); i < n; i += kFwdThreads) list[i] = tab->unit[o0 + i];
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1162,22 +1208,20 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap& tmQ, const CUte
   // kernel's outputs (Q, K, V, kv_valid_len) and writes O and LSE.
   grid_dependency_wait();
 
-  // Register budgets per warpgroup (RegBudget): they add up to 4 x 128, the
-  // launch's share.
-  using R = RegBudget<kTab>;
+  // Register budgets per warpgroup: they add up to 4 x 128, the launch's share.
   if (warp < 4) {
-    regs_set<R::kRoles>();
+    regs_set<kRegsRoles>();
     if (warp == 0) {
-      if (lane == 0) load_role<D, kF8>(sm, &tmQ, &tmK, &tmV, p, tab, w);
+      if (lane == 0) load_role<D, kF8, kTab>(sm, &tmQ, &tmK, &tmV, p, w);
     } else if (warp == 1) {
-      mma_role<D, kF8>(sm, tmem, p, tab, w);
+      mma_role<D, kF8, kTab>(sm, tmem, p, w);
     }
   } else if (warp < kEpiWarp0) {
-    regs_set<R::kSoftmax>();
-    softmax_role<D, kSplit, kF8>(sm, (warp - 4) >> 2, tmem, p, tab, w);
+    regs_set<kRegsSoftmax>();
+    softmax_role<D, kSplit, kF8, kTab>(sm, (warp - 4) >> 2, tmem, p, w);
   } else {
-    regs_set<R::kEpi>();
-    epilogue_role<D, kSplit, kF8>(sm, &tmO, tmem, p, tab, w);
+    regs_set<kRegsEpi>();
+    epilogue_role<D, kSplit, kF8, kTab>(sm, &tmO, tmem, p, w);
   }
   grid_launch_dependents();  // this thread has issued all of its work
 
@@ -1441,7 +1485,9 @@ bool schedule_wanted(int causal, const int32_t* kv_valid_len, int n_splits, int6
          n_units <= kTabMaxUnits && grid <= kTabMaxCtas;
 }
 
-void build_schedule(int BH, int n_pairs, int S_q, int S_kv, int D, int eb, int G, UnitTable* tab) {
+// Returns false (the launch then keeps the formula order) when some CTA would
+// be given more than kListMax units.
+bool build_schedule(int BH, int n_pairs, int S_q, int S_kv, int D, int eb, int G, UnitTable* tab) {
   const int n_units = BH * n_pairs;
   // kv steps of unit u (encoded as make_unit decodes it when causal)
   auto steps = [&](int u) {
@@ -1474,31 +1520,42 @@ void build_schedule(int BH, int n_pairs, int S_q, int S_kv, int D, int eb, int G
   }
   int pos = 0;
   for (int c = 0; c < G; ++c) {
+    if (lists[c].size() > static_cast<size_t>(kListMax)) return false;
     tab->off[c] = static_cast<uint16_t>(pos);
     for (const uint16_t u : lists[c]) tab->unit[pos++] = u;
   }
   tab->off[G] = static_cast<uint16_t>(pos);
+  return true;
 }
 
 // The last few schedules, by shape (a schedule is a pure function of it).
 struct SchedEntry {
   int key[7];
+  bool ok;  // build_schedule's result
   UnitTable tab;
 };
 std::mutex g_sched_mu;
 std::vector<SchedEntry> g_sched_cache;
 
-const UnitTable* schedule_for(int BH, int n_pairs, int S_q, int S_kv, int D, int eb, int G) {
+// Copies the schedule for this shape into *out, building and caching it on
+// first use; false when the shape has none (see build_schedule).  The copy is
+// made under the cache's lock: another thread may evict or move entries as
+// soon as it is released.
+bool schedule_for(int BH, int n_pairs, int S_q, int S_kv, int D, int eb, int G, UnitTable* out) {
   const int key[7] = {BH, n_pairs, S_q, S_kv, D, eb, G};
   std::lock_guard<std::mutex> lock(g_sched_mu);
   for (const SchedEntry& e : g_sched_cache)
-    if (std::equal(key, key + 7, e.key)) return &e.tab;
+    if (std::equal(key, key + 7, e.key)) {
+      if (e.ok) *out = e.tab;
+      return e.ok;
+    }
   if (g_sched_cache.size() >= 8) g_sched_cache.erase(g_sched_cache.begin());
   g_sched_cache.emplace_back();
   SchedEntry& e = g_sched_cache.back();
   std::copy(key, key + 7, e.key);
-  build_schedule(BH, n_pairs, S_q, S_kv, D, eb, G, &e.tab);
-  return &e.tab;
+  e.ok = build_schedule(BH, n_pairs, S_q, S_kv, D, eb, G, &e.tab);
+  if (e.ok) *out = e.tab;
+  return e.ok;
 }
 
 // Launches the attention kernel; with n_splits > 1 it writes fp32 partials to
@@ -1535,13 +1592,9 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* o, float
   const dim3 grid(static_cast<unsigned>(G));
   cudaError_t e;
   const dim3 block(kFwdThreads);
-  if (schedule_wanted(causal, kv_valid_len, n_splits, BH, S_kv, D, C::kEB, prm.n_units, G)) {
-    UnitTable tab;  // copied into the launch's parameters
-    {
-      const UnitTable* t = schedule_for(static_cast<int>(BH), prm.n_pairs, S_q, S_kv, D, C::kEB, G);
-      std::lock_guard<std::mutex> lock(g_sched_mu);  // the cache entry may be replaced by another thread
-      tab = *t;
-    }
+  UnitTable tab;  // copied into the launch's parameters
+  if (schedule_wanted(causal, kv_valid_len, n_splits, BH, S_kv, D, C::kEB, prm.n_units, G) &&
+      schedule_for(static_cast<int>(BH), prm.n_pairs, S_q, S_kv, D, C::kEB, G, &tab)) {
     e = launch_pdl(attn_fwd_sm103a_sched<D, kF8>, grid, block, C::kSmemBytes, stream, tq, tk, tv, to, prm, tab);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
   }
@@ -1807,6 +1860,25 @@ int attn_fwd_splitkv_suggest(int B, int H, int S_q, int S_kv, int D, int causal)
   const int64_t by_sms = (sms + units - 1) / units;
   const int64_t by_len = std::max<int64_t>(1, kv_tiles / 4);
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({by_sms, by_len, kMaxSplits})));
+}
+
+int attn_fwd_schedule(int B, int H, int S_q, int S_kv, int D, int elem_bytes, int sms, uint16_t* off,
+                      uint16_t* unit, int cap) {
+  if (B < 1 || H < 1 || S_q < 1 || S_kv < 1 || (D != 64 && D != 128) || (elem_bytes != 1 && elem_bytes != 2) ||
+      sms < 1 || off == nullptr || unit == nullptr)
+    return -1;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t n_pairs = (static_cast<int64_t>(S_q) + kRowsPerUnit - 1) / kRowsPerUnit;
+  if (BH * n_pairs > INT_MAX) return -1;
+  const int n_units = static_cast<int>(BH * n_pairs);
+  const int G = std::min(n_units, sms);
+  if (!schedule_wanted(1, nullptr, 1, BH, S_kv, D, elem_bytes, n_units, G)) return 0;
+  if (cap < n_units) return -1;
+  UnitTable tab;
+  if (!schedule_for(static_cast<int>(BH), static_cast<int>(n_pairs), S_q, S_kv, D, elem_bytes, G, &tab)) return 0;
+  std::copy(tab.off, tab.off + G + 1, off);
+  std::copy(tab.unit, tab.unit + n_units, unit);
+  return n_units;
 }
 
 attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
