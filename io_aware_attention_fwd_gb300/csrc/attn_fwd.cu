@@ -1677,6 +1677,7 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
   prm.BH = static_cast<int>(BH);
   prm.n_kv_tiles = (S_kv + kBN - 1) / kBN;
   prm.n_q_tiles = S_pad / kBM;
+  prm.head_group = bwd_head_group(S_q, D);
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   prm.scale = scale;
   prm.causal = causal;

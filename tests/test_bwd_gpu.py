@@ -147,3 +147,32 @@ def test_bwd_bench_size_sampled_heads(dev, causal, shape):
         ref = oracle.attention_bwd_f64(bits(q), bits(k), bits(v), bits(d_o), scale, causal)
         got = [x[b:b + 1, h:h + 1].float().cpu().numpy().astype(np.float64) for x in (dq, dk, dv)]
         compare_grads(got, ref)
+
+
+def test_bwd_causal_partial_head_group(dev):
+    """Causal CTAs run in groups of heads sized so that a group's fp32 dQ
+    accumulators fit in 32 MiB: at 5000 tokens and D = 128 that is 8 heads,
+    so 12 heads form one group of 8 and one of 4 (and the last tile is
+    ragged).  Heads from both groups are checked against the oracle."""
+    import torch
+    import io_aware_attention_fwd_gb300 as attn
+    B, H, S, D = 1, 12, 5000, 128
+    assert 16 * S * D * 4 > 32 << 20 >= 8 * S * D * 4
+    seed = 1260
+    scale = 1 / math.sqrt(D)
+    q, k, v = si.qkv_bf16_torch(seed, B, H, S, S, D, device=dev)
+    d_o = si.normal_bf16_torch(seed, 5, B * H * S * D, device=dev).view(B, H, S, D)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    attn.attn_fwd(q, k, v, o, lse, B, H, S, S, D, scale, True, None)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = attn.attn_bwd_workspace_bytes(B, H, S, D)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    attn.attn_bwd(q, k, v, o, lse, d_o, dq, dk, dv, B, H, S, S, D, scale, True, None, ws, nbytes)
+    torch.cuda.synchronize()
+    assert attn.attn_fwd_debug_status() == attn.ATTN_OK
+    for h in (0, 7, 8, 11):  # first and last head of each group
+        bits = lambda t: t[:, h:h + 1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        ref = oracle.attention_bwd_f64(bits(q), bits(k), bits(v), bits(d_o), scale, True)
+        got = [x[:, h:h + 1].float().cpu().numpy().astype(np.float64) for x in (dq, dk, dv)]
+        compare_grads(got, ref)
