@@ -397,6 +397,15 @@ def oracle_sample(w, q_bits, k_bits, v_bits, target_s, modes):
     return fl / dt / 1e12, dt, n, threads
 
 
+def extrapolated_step_s(w, tflops):
+    """Seconds the oracle would take for one whole step of workload ``w`` (all
+    rows, every mode) at the rate it reached on its sample: an
+    extrapolation, not a measurement."""
+    if not tflops or tflops <= 0:
+        return None
+    return sum(alg_flops(w, c) for c in w["modes"]) / (tflops * 1e12)
+
+
 def cpu_model():
     try:
         for line in Path("/proc/cpuinfo").read_text().splitlines():
@@ -435,7 +444,8 @@ def run_reference(args, w, rank):
         "data": "synthetic (seeded N(0,1) bf16 inputs)",
         "config": workload_config(args.workload, w, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": sample, "cpu": cpu_model()},
+                         "sample": sample, "cpu": cpu_model(),
+                         "extrapolated_full_step_s": extrapolated_step_s(w, value)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -663,6 +673,7 @@ def main():
                        f"each in modes {line['config']['modes']}, {dt:.1f} s of fp64 CPU time; "
                        f"TFLOP/s credited for exactly those rows"),
             "cpu": cpu_model(),
+            "extrapolated_full_step_s": extrapolated_step_s(w, tf),
         }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -158,6 +158,10 @@ def test_reference_arm_under_torchrun_world2():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    # the whole step at the sampled rate, labelled as an extrapolation
+    w = bench.WORKLOADS["b4_h16_s1024_d64"]
+    full = sum(bench.alg_flops(w, c) for c in w["modes"])
+    assert d["cpu_baseline"]["extrapolated_full_step_s"] == pytest.approx(full / (d["value"] * 1e12))
     # the same config object the GPU arm prints for this workload
     assert d["config"] == bench.workload_config("b4_h16_s1024_d64", bench.WORKLOADS["b4_h16_s1024_d64"], 2)
 
