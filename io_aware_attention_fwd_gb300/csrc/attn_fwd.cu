@@ -107,12 +107,15 @@ struct Cfg {
   static constexpr int kStatOff = kStageOff + 4 * kStagePanelBytes;  // float2 (m, l) [kQTiles][kBM]
   static constexpr int kBarOff = kStatOff + kQTiles * kBM * 8;
   // barriers: q_full | q_free[2] | full[kSlots] | empty[kSlots] | s_full[2] | p_full[2] |
-  //           o_done[2] | drain | turn | o_free[2] | epi[2]
-  static constexpr int kNumBars = 1 + kQTiles + 2 * kSlots + 3 * kQTiles + 2 + 2 * kQTiles;
+  //           o_done[2] | drain | turn | o_free[2] | epi[2] | p_half[2]
+  static constexpr int kNumBars = 1 + kQTiles + 2 * kSlots + 3 * kQTiles + 2 + 3 * kQTiles;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] tmem base, [1] abort flag, [2] listed units
   static constexpr int kListOff = kMiscOff + 16;           // uint16 [kListMax]: this CTA's units (host order)
   static constexpr int kSmemBytes = kListOff + 2 * kListMax + 1024;  // + slack for 1024 B alignment
   static constexpr int kOCol0 = kQTiles * kBN;             // first O column in TMEM
+  // bf16: the softmax hands P over in two halves of 64 keys, so the first
+  // half of P.V runs while the second half's exponentials are computed.
+  static constexpr bool kPHalves = !kF8;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -550,12 +553,12 @@ __device__ __forceinline__ void issue_qk(uint32_t pred, uint32_t d_tmem, uint64_
 // O[tmem] (+)= P[tmem] . V_tile[smem] over the 128 keys; every MMA consumes 32
 // bytes of each P row (8 TMEM columns) and kKeysPerStep rows of 128 bytes of
 // the MN-major V layout.
-template <int D, bool kF8>
+template <int D, bool kF8, int kK0 = 0, int kK1 = Cfg<D, kF8>::kPvSteps>
 __device__ __forceinline__ void issue_pv(uint32_t pred, uint32_t d_tmem, uint32_t p_tmem, uint64_t vd, uint32_t idesc,
                                          bool accumulate) {
   using C = Cfg<D, kF8>;
 #pragma unroll
-  for (int kk = 0; kk < C::kPvSteps; ++kk) {
+  for (int kk = kK0; kk < kK1; ++kk) {
     mma_ts_if<kF8>(pred, d_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
                    vd + static_cast<uint64_t>((kk * C::kKeysPerStep * 128) >> 4), idesc,
                    (accumulate || kk > 0) ? 1u : 0u);
@@ -617,6 +620,8 @@ struct Smem {
   // epilogue warpgroup hand-offs
   __device__ uint32_t bar_ofree(int t) const { return bar(3 + 4 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
   __device__ uint32_t bar_epi(int t) const { return bar(3 + 5 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
+  // the first half of P_t (keys 0-63) is in TMEM (kPHalves)
+  __device__ uint32_t bar_phalf(int t) const { return bar(3 + 6 * kQTiles + 2 * Cfg<D, kF8>::kSlots + t); }
 };
 
 // One work unit: two 128-row query tiles of one (batch, head).
@@ -843,12 +848,26 @@ __device__ void mma_role(const Smem<D, kF8>& sm, uint32_t tmem, const Params& p,
 #pragma unroll
       for (int t = 0; t < kQTiles; ++t) {
         if (!ok || j >= un.nkv[t]) continue;
-        ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_p(t), pc[t] & 1, w));
-        ++pc[t];
-        if (ok && j == 0 && k > 0) ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_ofree(t), (k - 1) & 1, w));
-        if (!ok) continue;
-        tc_fence_after();
-        issue_pv<D, kF8>(leader, tO[t], tS[t], vd0 + sv * kSlotStep, idesc_pv, j > 0);
+        if constexpr (C::kPHalves) {  // P.V over keys 0-63 as soon as that half of P is in TMEM
+          constexpr int kH = C::kPvSteps / 2;
+          ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_phalf(t), pc[t] & 1, w));
+          if (ok && j == 0 && k > 0) ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_ofree(t), (k - 1) & 1, w));
+          if (!ok) continue;
+          tc_fence_after();
+          issue_pv<D, kF8, 0, kH>(leader, tO[t], tS[t], vd0 + sv * kSlotStep, idesc_pv, j > 0);
+          ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_p(t), pc[t] & 1, w));
+          ++pc[t];
+          if (!ok) continue;
+          tc_fence_after();
+          issue_pv<D, kF8, kH, C::kPvSteps>(leader, tO[t], tS[t], vd0 + sv * kSlotStep, idesc_pv, true);
+        } else {
+          ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_p(t), pc[t] & 1, w));
+          ++pc[t];
+          if (ok && j == 0 && k > 0) ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_ofree(t), (k - 1) & 1, w));
+          if (!ok) continue;
+          tc_fence_after();
+          issue_pv<D, kF8>(leader, tO[t], tS[t], vd0 + sv * kSlotStep, idesc_pv, j > 0);
+        }
         tc_commit_if(leader, sm.bar_o(t));
         if (j + 1 < un.nkv[t]) {
           issue_qk<D, kF8>(leader, tS[t], qd[t], kd0 + skn * kSlotStep, idesc_s);
@@ -952,8 +971,36 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
       }
       const float mc = (m_c == -INFINITY) ? 0.f : m_c;
 
+      // Lazy correction: O is rescaled only when some row's max grew by > 2^8.
+      // (Kept in the softmax warps: every hand-off to a separate warpgroup
+      // measured slower than this rarely taken branch.)  It must land before
+      // this step's first P.V, which the P hand-off releases.
+      auto rescale_if_needed = [&]() {
+        if (!__any_sync(0xffffffffu, rescale_o)) return;
+        ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (cnt + j - 1) & 1, w));
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t tO = tmem + lane_off + C::kOCol0 + t * D;
+        const uint64_t a2 = pack_f32x2(alpha, alpha);
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float x0, x1;
+            unpack_f32x2(mul_f32x2(pack_f32x2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
+            o[i] = __float_as_uint(x0);
+            o[i + 1] = __float_as_uint(x1);
+          }
+          tmem_st32(tO + cc, o);
+        }
+        tmem_wait_st();
+      };
+
       // p = 2^(s*c - m): one FFMA and one MUFU.EX2 per score; the fp32 p
-      // feed the row sum, their bf16 pairs feed the P.V MMA.
+      // feed the row sum, their packed values feed the P.V MMA.
       uint32_t pk[C::kPCols];
       float sum0 = 0.f, sum1 = 0.f;
       if constexpr (kF8) {  // P as e4m3, four per TMEM column
@@ -967,48 +1014,40 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
           sum1 += b + f;
           pk[i] = pack_e4m3x4(a, b, e, f);
         }
-      } else {  // P as bf16, two per TMEM column
 #pragma unroll
-        for (int i = 0; i < kBN / 2; ++i) {
+        for (int cc = 0; cc < C::kPCols; cc += 32) tmem_st32(tS + cc, pk + cc);
+        if (C::kTurn) mbar_arrive(sm.bar_turn());
+        tmem_wait_st();
+        rescale_if_needed();
+      } else {  // P as bf16, two per TMEM column, handed over in two halves
+        static_assert(C::kPHalves && C::kPCols == 64, "bf16 P: two halves of 32 TMEM columns");
+#pragma unroll
+        for (int i = 0; i < kBN / 4; ++i) {
           const float a = ex2_approx(fmaf(s[2 * i], c, -mc));
           const float b = ex2_approx(fmaf(s[2 * i + 1], c, -mc));
           sum0 += a;
           sum1 += b;
           pk[i] = pack_bf16x2(a, b);
         }
+        tmem_st32(tS, pk);
+        tmem_wait_st();
+        rescale_if_needed();
+        tc_fence_before();
+        mbar_arrive(sm.bar_phalf(t));  // P.V may start on keys 0-63
+#pragma unroll
+        for (int i = kBN / 4; i < kBN / 2; ++i) {
+          const float a = ex2_approx(fmaf(s[2 * i], c, -mc));
+          const float b = ex2_approx(fmaf(s[2 * i + 1], c, -mc));
+          sum0 += a;
+          sum1 += b;
+          pk[i] = pack_bf16x2(a, b);
+        }
+        tmem_st32(tS + 32, pk + 32);
+        if (C::kTurn) mbar_arrive(sm.bar_turn());
+        tmem_wait_st();
       }
       const float sa = sum0, sb = sum1;
       l = l * alpha + (sa + sb);
-#pragma unroll
-      for (int cc = 0; cc < C::kPCols; cc += 32) tmem_st32(tS + cc, pk + cc);
-      if (C::kTurn) mbar_arrive(sm.bar_turn());
-      tmem_wait_st();
-      // Lazy correction: O is rescaled only when some row's max grew by > 2^8.
-      // (Kept in the softmax warps: every hand-off to a separate warpgroup
-      // measured slower than this rarely taken branch.)
-      if (__any_sync(0xffffffffu, rescale_o)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_o(t), (cnt + j - 1) & 1, w));
-        if (ok) {
-          tc_fence_after();
-          const uint32_t tO = tmem + lane_off + C::kOCol0 + t * D;
-          const uint64_t a2 = pack_f32x2(alpha, alpha);
-#pragma unroll 1
-          for (int cc = 0; cc < D; cc += 32) {
-            uint32_t o[32];
-            tmem_ld32(tO + cc, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float x0, x1;
-              unpack_f32x2(mul_f32x2(pack_f32x2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
-              o[i] = __float_as_uint(x0);
-              o[i + 1] = __float_as_uint(x1);
-            }
-            tmem_st32(tO + cc, o);
-          }
-          tmem_wait_st();
-        }
-      }
       tc_fence_before();
       mbar_arrive(sm.bar_p(t));
     }
@@ -1178,6 +1217,7 @@ __device__ __forceinline__ void attn_fwd_body(const CUtensorMap& tmQ, const CUte
       mbar_init(sm.bar_o(t), 1);
       mbar_init(sm.bar_ofree(t), kBM);  // the four epilogue warps
       mbar_init(sm.bar_epi(t), kBM);    // the tile's softmax threads
+      mbar_init(sm.bar_phalf(t), kBM);  // the tile's softmax threads
     }
     mbar_init(sm.bar_drain(), 1);
     mbar_init(sm.bar_turn(), kBM);
