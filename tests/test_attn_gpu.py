@@ -94,6 +94,21 @@ def test_long_causal_host_schedule_ragged(dev, D, S, H):
     parity.check_against_oracle(q, k, v, 1 / math.sqrt(D), True, rows=rows)
 
 
+@pytest.mark.parametrize("D,S_q,S_kv,H", [(128, 3000, 20000, 16), (128, 12000, 8200, 32)])
+def test_long_causal_host_schedule_unequal_lengths(dev, D, S_q, S_kv, H):
+    # The host-computed order with S_q != S_kv: the causal mask is aligned top
+    # left (key j is allowed for query i when j <= i), so with S_kv > S_q the
+    # last keys are never seen, and with S_q > S_kv the rows past S_kv see
+    # every key.
+    import io_aware_attention_fwd_gb300 as attn
+    assert H * S_kv * D * 2 * 2 > 64 << 20
+    assert attn.attn_fwd_schedule(1, H, S_q, S_kv, D, 2, 152) is not None
+    q, k, v = qkv(960 + S_q % 97, 1, H, S_q, S_kv, D)
+    rows = parity.sampled_rows(960 + S_q % 97, 1, H, S_q, 48,
+                               must_include=[0, 1, 127, 128, min(S_q, S_kv) - 1, S_q - 1])
+    parity.check_against_oracle(q, k, v, 1 / math.sqrt(D), True, rows=rows)
+
+
 # --- edge cases ----------------------------------------------------------------
 
 @pytest.mark.parametrize("D", [64, 128])
