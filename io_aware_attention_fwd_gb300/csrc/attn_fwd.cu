@@ -928,10 +928,12 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
       // bf16 at D = 128: the two softmax warpgroups take turns.  The CTA's
       // softmax steps are ordered per unit, per kv step, tile 0 before tile 1,
       // and step n starts its exponentials only once step n - 1 has finished
-      // its own, so each runs alone on the SM sub-partitions it shares with
-      // the other warpgroup while the tensor core serves the other query
-      // tile.  (Measured: +2-3% there; at D = 64 and with e4m3 operands the
-      // MMAs are too short for the alternation to pay, and it costs ~8%.)
+      // the first half of its own (keys 0-63), so the two warpgroups' bursts
+      // of exponentials overlap by half instead of fully, while the tensor
+      // core serves the other query tile.  (Measured on GB300: handing the
+      // turn over after the first half instead of after both was 3-8% faster
+      // at 4k-32k; at D = 64 and with e4m3 operands the MMAs are too short for
+      // the alternation to pay, and it costs ~8%.)
       const int step = sbase + min(j, n0) + min(j, n1) + ((t == 1 && j < n0) ? 1 : 0);
       ok = __all_sync(0xffffffffu, mbar_wait(sm.bar_s(t), (cnt + j) & 1, w) &&
                                        (!C::kTurn || step == 0 || mbar_wait(sm.bar_turn(), (step - 1) & 1, w)));
@@ -1031,6 +1033,7 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
           pk[i] = pack_bf16x2(a, b);
         }
         tmem_st32(tS, pk);
+        if (C::kTurn) mbar_arrive(sm.bar_turn());
         tmem_wait_st();
         rescale_if_needed();
         tc_fence_before();
@@ -1044,7 +1047,6 @@ __device__ void softmax_role(const Smem<D, kF8>& sm, int t, uint32_t tmem, const
           pk[i] = pack_bf16x2(a, b);
         }
         tmem_st32(tS + 32, pk + 32);
-        if (C::kTurn) mbar_arrive(sm.bar_turn());
         l = l * alpha + (sum0 + sum1);
         tmem_wait_st();
       }
