@@ -109,6 +109,50 @@ def test_long_causal_host_schedule_unequal_lengths(dev, D, S_q, S_kv, H):
     parity.check_against_oracle(q, k, v, 1 / math.sqrt(D), True, rows=rows)
 
 
+
+@pytest.mark.parametrize("D,S,H", [(128, 8192, 32), (64, 17000, 16)])
+def test_host_schedule_is_bit_identical_to_the_formula_order(dev, D, S, H):
+    # The host-built order only changes which CTA computes a unit and when;
+    # every row's arithmetic is the same.  A launch with kv_valid_len = S_kv
+    # for every batch computes the same attention but keeps the formula
+    # (longest-first) order, so O and LSE must agree bit for bit.
+    import torch
+    import io_aware_attention_fwd_gb300 as attn
+    assert attn.attn_fwd_schedule(1, H, S, S, D, 2, 152) is not None
+    q, k, v = (parity.to_device(x, dev) for x in qkv(970 + D, 1, H, S, S, D))
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    l1 = torch.empty((1, H, S), dtype=torch.float32, device=dev)
+    l2 = torch.empty_like(l1)
+    full = torch.tensor([S], dtype=torch.int32, device=dev)
+    attn.attn_fwd(q, k, v, o1, l1, 1, H, S, S, D, 1 / math.sqrt(D), True, None)
+    attn.attn_fwd(q, k, v, o2, l2, 1, H, S, S, D, 1 / math.sqrt(D), True, full)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+
+def test_host_schedule_is_bit_identical_to_the_formula_order_e4m3(dev):
+    # The same check for the e4m3 kernel (its K + V here: 98 MB > 64 MiB).
+    import torch
+    import io_aware_attention_fwd_gb300 as attn
+    B, H, S, D = 1, 32, 12000, 128
+    assert attn.attn_fwd_schedule(B, H, S, S, D, 1, 152) is not None
+    q, k, v = (si.normal_e4m3_torch(980, tid, B * H * S * D, 16.0, device=dev).view(B, H, S, D)
+               for tid in (si.TID_Q, si.TID_K, si.TID_V))
+    o1 = torch.empty((B, H, S, D), dtype=torch.bfloat16, device=dev)
+    o2 = torch.empty_like(o1)
+    l1 = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    l2 = torch.empty_like(l1)
+    full = torch.tensor([S], dtype=torch.int32, device=dev)
+    ds = 1.0 / 16.0
+    attn.attn_fwd_fp8(q, k, v, o1, l1, B, H, S, S, D, 1 / math.sqrt(D), ds, ds, ds, True, None)
+    attn.attn_fwd_fp8(q, k, v, o2, l2, B, H, S, S, D, 1 / math.sqrt(D), ds, ds, ds, True, full)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
 # --- edge cases ----------------------------------------------------------------
 
 @pytest.mark.parametrize("D", [64, 128])
