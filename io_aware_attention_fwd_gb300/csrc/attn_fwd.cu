@@ -1331,8 +1331,17 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
   const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t step = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t row = first; row < rows; row += step) {
-    float mx = -INFINITY;
-    for (int k = lane; k < n_parts; k += 32) mx = fmaxf(mx, __ldg(lse_parts + k * part_stride_rows + row));
+    const float* src = o_parts + row * D + lane * kPer;
+    // The first batch of partial rows is requested together with the LSEs,
+    // so the two loads overlap instead of following each other.
+    Vec v0[kBatch];
+    const int n0 = min(kBatch, n_parts);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (u < n0) v0[u] = __ldg(reinterpret_cast<const Vec*>(src + u * part_stride_rows * D));
+    const float lse_mine = lane < n_parts ? __ldg(lse_parts + lane * part_stride_rows + row) : -INFINITY;
+    float mx = lse_mine;
+    for (int k = lane + 32; k < n_parts; k += 32) mx = fmaxf(mx, __ldg(lse_parts + k * part_stride_rows + row));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     float acc[kPer];
@@ -1340,12 +1349,24 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
     float wsum = 0.f;  // this lane's share of the weight sum
     if (mx > -INFINITY) {
-      const float* src = o_parts + row * D + lane * kPer;
       for (int k0 = 0; k0 < n_parts; k0 += 32) {
         const int cnt = min(32, n_parts - k0);
-        const float w_mine = lane < cnt ? expf(__ldg(lse_parts + (k0 + lane) * part_stride_rows + row) - mx) : 0.f;
+        const float w_mine =
+            lane < cnt ? expf((k0 == 0 ? lse_mine : __ldg(lse_parts + (k0 + lane) * part_stride_rows + row)) - mx)
+                       : 0.f;
         wsum += w_mine;
         int j = 0;
+        if (k0 == 0) {  // the batch already in registers
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            if (u >= n0) break;
+            const float wk = __shfl_sync(0xffffffffu, w_mine, u);
+            const float* f = reinterpret_cast<const float*>(&v0[u]);
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[e] += wk * f[e];
+          }
+          j = n0;
+        }
         for (; j + kBatch <= cnt; j += kBatch) {
           Vec v[kBatch];
 #pragma unroll
